@@ -1,0 +1,205 @@
+"""Oracle for the speculative-decoding verify/accept step -- TEST INFRASTRUCTURE.
+
+A plain fp64, single-threaded CPU restatement (``oracle.c``) of the rule the
+pages define, with a ctypes wrapper over numpy arrays.  Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference leg use
+it; the product library never imports it and shares no code with it.
+
+Sources: "[논문 리뷰] Fast Inference from Transformers via Speculative
+Decoding", section 2 (accept with min(1, p/q), residual max(0, p-q), bonus
+token); "Speculative Decoding and EAGLE", section "정확성 규칙" (r < p/q, the
+residual, the greedy case); "Progressive Tree Drafting", section "검증"
+(greedy and sampling tree acceptance).
+
+Array conventions: logits are numpy ``float32`` (fp32) or ``uint16`` holding
+bfloat16 bit patterns; draft probabilities are ``float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+F32, BF16 = 0, 1
+DRAFT_PROBS, DRAFT_LOGITS = 0, 1
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` next to it (gcc, no FMA contraction,
+    so x86_64 and aarch64 hosts compute identical doubles)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math",
+                        "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        vp, i32p, f32p, f64p, u64p = (ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32),
+                                      ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_uint64))
+        ci, u64 = ctypes.c_int, ctypes.c_uint64
+        lib.oracle_philox4x64_10.argtypes = [u64p, u64p, u64p]
+        lib.oracle_philox4x64_10.restype = None
+        lib.oracle_verify_chain_u.argtypes = [vp, ci, vp, ci, ci, i32p, f32p, ci, ci, ci,
+                                              f64p, f64p, i32p, i32p, f32p, f64p]
+        lib.oracle_verify_chain.argtypes = [vp, ci, vp, ci, ci, i32p, f32p, ci, ci, ci,
+                                            u64, u64, i32p, i32p, i32p, f32p, f64p]
+        lib.oracle_greedy_accept.argtypes = [vp, ci, i32p, ci, ci, ci, i32p, i32p]
+        lib.oracle_verify_tree_u.argtypes = [vp, ci, vp, ci, ci, i32p, i32p, f32p, ci, ci, ci, ci,
+                                             f64p, f64p, i32p, i32p, i32p, f64p]
+        lib.oracle_verify_tree.argtypes = [vp, ci, vp, ci, ci, i32p, i32p, f32p, ci, ci, ci, ci,
+                                           u64, u64, i32p, i32p, i32p, i32p, f64p]
+        for name in ("oracle_verify_chain_u", "oracle_verify_chain", "oracle_greedy_accept",
+                     "oracle_verify_tree_u", "oracle_verify_tree"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a, ctype):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _logits_dtype(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"logits must be float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def philox4x64_10(counter, key) -> np.ndarray:
+    """One Philox4x64-10 block for a 4-word counter and a 2-word key."""
+    lib = _load()
+    c = _c(np.asarray(counter, dtype=np.uint64), np.uint64)
+    k = _c(np.asarray(key, dtype=np.uint64), np.uint64)
+    out = np.zeros(4, dtype=np.uint64)
+    lib.oracle_philox4x64_10(_ptr(c, ctypes.c_uint64), _ptr(k, ctypes.c_uint64),
+                             _ptr(out, ctypes.c_uint64))
+    return out
+
+
+def _draft_args(draft, draft_kind):
+    if draft is None:
+        return None, F32
+    if draft_kind == DRAFT_PROBS:
+        if draft.dtype != np.float32:
+            raise TypeError("draft probabilities must be float32")
+        return draft, F32
+    return draft, _logits_dtype(draft)
+
+
+def verify_chain(target, draft, draft_tokens, temperature, seed, offset,
+                 draft_kind=DRAFT_LOGITS, row_id=None, uniforms=None):
+    """Chain verify.  target [B][K+1][V], draft [B][K][V], draft_tokens [B][K],
+    temperature [B].  ``uniforms=(r, u)`` ([B][K], [B][K+1] float64) replaces the
+    Philox stream.  Returns dict(tokens, count, accept_prob, margin, n_invalid)."""
+    lib = _load()
+    target = np.ascontiguousarray(target)
+    B, K1, V = target.shape
+    K = K1 - 1
+    tdt = _logits_dtype(target)
+    draft = None if draft is None else np.ascontiguousarray(draft)
+    draft, ddt = _draft_args(draft, draft_kind)
+    if draft is not None and draft.shape != (B, K, V):
+        raise ValueError(f"draft shape {draft.shape} != {(B, K, V)}")
+    toks = _c(draft_tokens, np.int32).reshape(B, K)
+    temps = _c(temperature, np.float32).reshape(B)
+    out_t = np.full((B, K + 1), -1, np.int32)
+    out_c = np.zeros(B, np.int32)
+    out_ap = np.full((B, max(K, 1)), -1, np.float32)
+    out_m = np.zeros(B, np.float64)
+    dptr = None if draft is None else draft.ctypes.data
+    if uniforms is None:
+        rid = None if row_id is None else _c(row_id, np.int32)
+        n = lib.oracle_verify_chain(target.ctypes.data, tdt, dptr, ddt, draft_kind,
+                                    _ptr(toks, ctypes.c_int32), _ptr(temps, ctypes.c_float), B, K, V,
+                                    ctypes.c_uint64(seed), ctypes.c_uint64(offset),
+                                    _ptr(rid, ctypes.c_int32), _ptr(out_t, ctypes.c_int32),
+                                    _ptr(out_c, ctypes.c_int32), _ptr(out_ap, ctypes.c_float),
+                                    _ptr(out_m, ctypes.c_double))
+    else:
+        r = _c(uniforms[0], np.float64).reshape(B, K) if K > 0 else np.zeros((B, 1))
+        u = _c(uniforms[1], np.float64).reshape(B, K + 1)
+        n = lib.oracle_verify_chain_u(target.ctypes.data, tdt, dptr, ddt, draft_kind,
+                                      _ptr(toks, ctypes.c_int32), _ptr(temps, ctypes.c_float), B, K, V,
+                                      _ptr(r, ctypes.c_double), _ptr(u, ctypes.c_double),
+                                      _ptr(out_t, ctypes.c_int32), _ptr(out_c, ctypes.c_int32),
+                                      _ptr(out_ap, ctypes.c_float), _ptr(out_m, ctypes.c_double))
+    return dict(tokens=out_t, count=out_c, accept_prob=out_ap[:, :K], margin=out_m, n_invalid=n)
+
+
+def greedy_accept(target, draft_tokens):
+    """Greedy acceptance (argmax rule) for every row.  Returns dict(tokens, count)."""
+    lib = _load()
+    target = np.ascontiguousarray(target)
+    B, K1, V = target.shape
+    K = K1 - 1
+    toks = _c(draft_tokens, np.int32).reshape(B, K)
+    out_t = np.full((B, K + 1), -1, np.int32)
+    out_c = np.zeros(B, np.int32)
+    n = lib.oracle_greedy_accept(target.ctypes.data, _logits_dtype(target), _ptr(toks, ctypes.c_int32),
+                                 B, K, V, _ptr(out_t, ctypes.c_int32), _ptr(out_c, ctypes.c_int32))
+    return dict(tokens=out_t, count=out_c, n_invalid=n)
+
+
+def verify_tree(target, draft, node_tokens, parent, temperature, max_depth, seed, offset,
+                draft_kind=DRAFT_LOGITS, row_id=None, uniforms=None):
+    """Tree verify.  target/draft [B][N+1][V] (row 0 = root, row i+1 = after node i),
+    node_tokens/parent [B][N].  ``uniforms=(r, u)`` ([B][N], [B][N+1]) replaces the
+    Philox stream.  Returns dict(tokens, count, path, margin, n_invalid)."""
+    lib = _load()
+    target = np.ascontiguousarray(target)
+    B, N1, V = target.shape
+    N = N1 - 1
+    tdt = _logits_dtype(target)
+    draft = None if draft is None else np.ascontiguousarray(draft)
+    draft, ddt = _draft_args(draft, draft_kind)
+    if draft is not None and draft.shape != (B, N + 1, V):
+        raise ValueError(f"draft shape {draft.shape} != {(B, N + 1, V)}")
+    toks = _c(node_tokens, np.int32).reshape(B, N)
+    par = _c(parent, np.int32).reshape(B, N)
+    temps = _c(temperature, np.float32).reshape(B)
+    D = int(max_depth)
+    out_t = np.full((B, D + 1), -1, np.int32)
+    out_c = np.zeros(B, np.int32)
+    out_p = np.full((B, max(D, 1)), -1, np.int32)
+    out_m = np.zeros(B, np.float64)
+    dptr = None if draft is None else draft.ctypes.data
+    if uniforms is None:
+        rid = None if row_id is None else _c(row_id, np.int32)
+        n = lib.oracle_verify_tree(target.ctypes.data, tdt, dptr, ddt, draft_kind,
+                                   _ptr(toks, ctypes.c_int32), _ptr(par, ctypes.c_int32),
+                                   _ptr(temps, ctypes.c_float), B, N, V, D,
+                                   ctypes.c_uint64(seed), ctypes.c_uint64(offset),
+                                   _ptr(rid, ctypes.c_int32), _ptr(out_t, ctypes.c_int32),
+                                   _ptr(out_c, ctypes.c_int32), _ptr(out_p, ctypes.c_int32),
+                                   _ptr(out_m, ctypes.c_double))
+    else:
+        r = _c(uniforms[0], np.float64).reshape(B, N) if N > 0 else np.zeros((B, 1))
+        u = _c(uniforms[1], np.float64).reshape(B, N + 1)
+        n = lib.oracle_verify_tree_u(target.ctypes.data, tdt, dptr, ddt, draft_kind,
+                                     _ptr(toks, ctypes.c_int32), _ptr(par, ctypes.c_int32),
+                                     _ptr(temps, ctypes.c_float), B, N, V, D,
+                                     _ptr(r, ctypes.c_double), _ptr(u, ctypes.c_double),
+                                     _ptr(out_t, ctypes.c_int32), _ptr(out_c, ctypes.c_int32),
+                                     _ptr(out_p, ctypes.c_int32), _ptr(out_m, ctypes.c_double))
+    return dict(tokens=out_t, count=out_c, path=out_p[:, :D], margin=out_m, n_invalid=n)
