@@ -1,0 +1,168 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding verify library.
+ *
+ * The library implements the target-side verify/accept step of speculative
+ * decoding: given the target model's logits at the K+1 drafted positions, the
+ * draft distribution and the K drafted tokens, it decides which drafted tokens
+ * are kept and emits one more token (a replacement or a bonus token).
+ *
+ * Defining passages (page title, section):
+ *  - "[논문 리뷰] Fast Inference from Transformers via Speculative Decoding"
+ *    (review of Leviathan et al., ICML 2023), section 2 "제안 방법": Step 3
+ *    "Accept/Reject" (left to right, acceptance probability min(1, p(x)/q(x)),
+ *    replacement from max(0, p-q)/sum max(0, p-q) at the first rejection, later
+ *    drafts discarded, 1..K+1 tokens per round).
+ *  - "Speculative Decoding and EAGLE", sections "개념" (bonus token when all K
+ *    pass) and "정확성 규칙 (The Exactness Rule)" (r < p/q; residual
+ *    (p-q)+/||(p-q)+||_1; the greedy case accepts iff argmax(p) == x_t, else
+ *    emits argmax(p) and stops); section "트리 어텐션 검증" (the longest
+ *    accepted branch of a draft tree).
+ *  - "Progressive Tree Drafting" summary, section "검증 (Verification)":
+ *    greedy tree acceptance (an edge is accepted when the verified token equals
+ *    a child) and sampling acceptance without replacement from normalised
+ *    probabilities.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named as device arrays are caller-owned device memory; the library
+ *    never allocates, frees or retains them.  Arrays are dense and row-major in
+ *    the order their shapes are written.  Logits may be fp32 or bf16 (SV_F32 /
+ *    SV_BF16); draft probabilities are fp32.
+ *  - p = softmax(logits / T) per row; T <= 0 (or NaN) selects the greedy rule for
+ *    that batch row.  A draft given as logits uses the same T; a draft given as
+ *    probabilities is used as given (it must be a distribution).
+ *  - Randomness: Philox4x64-10 with counter {slot, b, offset, 0} and key
+ *    {seed, 0}, b the batch row index within the call.  Word 0 of slot k is the
+ *    accept uniform of chain position k (tree: of node k); word 1 of slot k is the
+ *    draw uniform at chain position k (tree: at distribution row k).  A uniform
+ *    is (w >> 40) * 2^-24.  The caller advances `offset` (or `seed`) per round.
+ *  - Acceptance is r < p(x)/q(x); q(x) == 0 accepts iff p(x) > 0.  Replacement
+ *    and bonus draws are inverse-CDF draws: the smallest index i whose prefix
+ *    sum C_i exceeds u * Z, Z the total weight.  A residual with zero mass falls
+ *    back to p.  argmax ties resolve to the lowest index.
+ *  - Arithmetic is fp32 on the device.  Results match an fp64 evaluation of the
+ *    same rule except where a decision lies within fp32 rounding of its boundary.
+ *  - Execution is asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *    is the legacy default stream).  Argument errors are detected on the host and
+ *    returned before anything is launched.  Launch failures return SV_ERR_CUDA.
+ *  - Per-row data errors do not fail the call: a batch row whose read logits
+ *    contain NaN or +inf or are all -inf, whose tokens lie outside [0, V), whose
+ *    draft probability at a drafted token is negative or not finite, or whose
+ *    parent array is malformed, gets out_count[b] = 0 and all output slots -1.
+ *    A valid row always has out_count[b] >= 1.
+ *  - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SV_API __attribute__((visibility("default")))
+#else
+#define SV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1, /* a size, pointer, dtype or kind argument is invalid */
+    SV_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles (size limits, device) */
+    SV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    SV_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up; the workspace must be re-zeroed */
+    SV_ERR_BAD_INPUT = 5    /* reserved for data errors reported through a status query */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+typedef enum { SV_DRAFT_PROBS = 0, SV_DRAFT_LOGITS = 1 } sv_draft_kind;
+
+/*
+ * Bytes of device workspace spec_verify_chain may use for B batch rows, K drafts
+ * and vocabulary V.  The caller zero-fills the workspace once before its first
+ * use; every successful call leaves it zeroed again.  Passing a smaller (or NULL)
+ * workspace is allowed and selects a path that needs none.
+ */
+SV_API size_t spec_verify_workspace_size(int B, int K, int V);
+
+/*
+ * Chain verify (sampling and greedy rows mixed by temperature).
+ *   target_logits  device [B][K+1][V], dtype tdt.  Row k is the target's next-token
+ *                  logits at chain position k (k = K: the bonus position).
+ *   draft          device [B][K][V]: SV_DRAFT_PROBS -> fp32 probabilities q_k;
+ *                  SV_DRAFT_LOGITS -> logits of dtype ddt, q_k = softmax(row / T).
+ *                  Not read for greedy rows; required (non-NULL) when K > 0.
+ *   draft_tokens   device int32 [B][K], the drafted tokens x_0..x_{K-1}.
+ *   temperature    device fp32 [B].
+ *   B >= 0, 0 <= K <= 64, 1 <= V <= 1<<24.
+ *   seed, offset   Philox key word and counter word (see conventions).
+ *   out_tokens     device int32 [B][K+1]: accepted drafts, then the replacement or
+ *                  bonus token; unused slots are -1.
+ *   out_count      device int32 [B]: number of valid entries in out_tokens[b]
+ *                  (1..K+1; 0 for an invalid row).
+ *   out_accept_prob  nullable device fp32 [B][K]: min(1, p_k(x_k)/q_k(x_k)) for every
+ *                  position up to and including the first rejection (greedy rows:
+ *                  1 for a match, 0 for the mismatch); -1 for positions never
+ *                  evaluated.
+ *   workspace, ws_bytes  optional scratch (see spec_verify_workspace_size).
+ * Rows after the first rejection are never read.
+ */
+SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt,
+                            const void *draft, sv_dtype ddt, sv_draft_kind dk,
+                            const int32_t *draft_tokens, const float *temperature,
+                            int B, int K, int V, uint64_t seed, uint64_t offset,
+                            int32_t *out_tokens, int32_t *out_count, float *out_accept_prob,
+                            void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Greedy acceptance (the temperature-0 rule) for every row:
+ *   target_logits device [B][K+1][V] (tdt), draft_tokens device int32 [B][K];
+ *   out_tokens device int32 [B][K+1], out_count device int32 [B].
+ * Accepts x_k while x_k == argmax(row k); emits argmax of the first mismatching row
+ * (or of row K when all match).  No draft distribution is read.
+ */
+SV_API sv_status spec_greedy_accept(const void *target_logits, sv_dtype tdt, const int32_t *draft_tokens,
+                             int B, int K, int V, int32_t *out_tokens, int32_t *out_count,
+                             void *stream);
+
+/*
+ * Tree verify.
+ *   target_logits  device [B][N+1][V] (tdt): row 0 is the root's next-token logits,
+ *                  row i+1 the next-token logits after node i.
+ *   draft          device [B][N+1][V], the same row layout (probs fp32 or logits ddt);
+ *                  row r is the draft distribution the children of that row's node
+ *                  were proposed from.  Not read for greedy rows.
+ *   node_tokens    device int32 [B][N]; parent device int32 [B][N] with parent[i] in
+ *                  {-1} u [0, i) (-1: child of the root).  Children of a node are tried
+ *                  in increasing node index.
+ *   temperature    device fp32 [B].  1 <= N <= 1024, 1 <= max_depth <= 64, max_depth at
+ *                  least the depth of every node (else the row is invalid).
+ *   out_tokens     device int32 [B][max_depth+1]: the accepted node tokens along the
+ *                  path, then the final drawn (or argmax) token; -1 padded.
+ *   out_count      device int32 [B] (1..depth+1; 0 for an invalid row).
+ *   out_path       device int32 [B][max_depth]: accepted node indices, -1 padded.
+ * Greedy rows descend into the lowest-index child whose token equals the argmax of
+ * the current row.  Sampling rows try the children in order with acceptance
+ * r < p(x)/q(x); after a rejection p <- (p - q)+ / |(p - q)+|_1 (kept if that mass
+ * is zero), q(x) <- 0 and q is renormalised.  With no child accepted, or at a
+ * leaf, the last token is drawn from the current p.
+ */
+SV_API sv_status spec_verify_tree(const void *target_logits, sv_dtype tdt,
+                           const void *draft, sv_dtype ddt, sv_draft_kind dk,
+                           const int32_t *node_tokens, const int32_t *parent,
+                           const float *temperature, int B, int N, int V, int max_depth,
+                           uint64_t seed, uint64_t offset,
+                           int32_t *out_tokens, int32_t *out_count, int32_t *out_path,
+                           void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+SV_API const char *spec_verify_status_string(sv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,200 @@
+"""GB300 (sm_103a) speculative-decoding verify/accept library -- Python binding.
+
+A thin ctypes layer over ``libspecverify.so`` (C ABI: ``include/spec_verify.h``).
+Each function carries the name of the C entry point it calls and only marshals
+arguments: torch tensors become device pointers, the current torch stream
+becomes the launch stream, outputs are allocated with torch when not given.
+Every step of the verify path runs in the library's CUDA kernels; there is no
+fallback -- a missing library raises.
+
+Build the library with ``python -m speculative_decoding_verification_53_gb300.build``
+(or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_TIMEOUT, SV_ERR_BAD_INPUT = range(6)
+SV_F32, SV_BF16 = 0, 1
+SV_DRAFT_PROBS, SV_DRAFT_LOGITS = 0, 1
+
+EXPORTS = ("spec_verify_workspace_size", "spec_verify_chain", "spec_greedy_accept", "spec_verify_tree",
+           "spec_verify_status_string")
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    """A non-zero sv_status returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {spec_verify_status_string(status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with argument types set (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m speculative_decoding_verification_53_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, ci, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+    L.spec_verify_workspace_size.argtypes = [ci, ci, ci]
+    L.spec_verify_workspace_size.restype = sz
+    L.spec_verify_chain.argtypes = [vp, ci, vp, ci, ci, vp, vp, ci, ci, ci, u64, u64, vp, vp, vp, vp, sz, vp]
+    L.spec_verify_chain.restype = ci
+    L.spec_greedy_accept.argtypes = [vp, ci, vp, ci, ci, ci, vp, vp, vp]
+    L.spec_greedy_accept.restype = ci
+    L.spec_verify_tree.argtypes = [vp, ci, vp, ci, ci, vp, vp, vp, ci, ci, ci, ci, u64, u64, vp, vp, vp, vp]
+    L.spec_verify_tree.restype = ci
+    L.spec_verify_status_string.argtypes = [ci]
+    L.spec_verify_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def spec_verify_status_string(status: int) -> str:
+    return lib().spec_verify_status_string(int(status)).decode()
+
+
+def spec_verify_workspace_size(B: int, K: int, V: int) -> int:
+    return int(lib().spec_verify_workspace_size(int(B), int(K), int(V)))
+
+
+# ---------------------------------------------------------------- helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _kind(draft_kind) -> int:
+    if draft_kind in ("probs", SV_DRAFT_PROBS):
+        return SV_DRAFT_PROBS
+    if draft_kind in ("logits", SV_DRAFT_LOGITS):
+        return SV_DRAFT_LOGITS
+    raise ValueError("draft_kind must be 'probs' or 'logits'")
+
+
+# ------------------------------------------------------------ entry points
+
+def spec_verify_chain(target_logits, draft, draft_tokens, temperature, seed: int, offset: int, *,
+                      draft_kind, out_tokens=None, out_count=None, out_accept_prob=None,
+                      want_accept_prob: bool = False, workspace=None, stream=None):
+    """Chain verify.  target_logits [B][K+1][V] (fp32/bf16), draft [B][K][V] (probs fp32 or
+    logits), draft_tokens int32 [B][K], temperature fp32 [B] (T <= 0: greedy row).
+    Returns (out_tokens int32 [B][K+1], out_count int32 [B], out_accept_prob fp32 [B][K] or None)."""
+    torch = _torch()
+    _dev(target_logits, "target_logits")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    dk = _kind(draft_kind)
+    _dev(draft, "draft")
+    _dev(draft_tokens, "draft_tokens", torch.int32)
+    _dev(temperature, "temperature", torch.float32)
+    ddt = SV_F32 if draft is None else _dtype_code(draft)
+    if draft is not None and tuple(draft.shape) != (B, K, V):
+        raise ValueError(f"draft shape {tuple(draft.shape)} != {(B, K, V)}")
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_count is None:
+        out_count = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_accept_prob is None and want_accept_prob:
+        out_accept_prob = torch.empty((B, K), dtype=torch.float32, device=dev)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    st = lib().spec_verify_chain(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), ddt, dk,
+                                 _ptr(draft_tokens), _ptr(temperature), B, K, V, int(seed), int(offset),
+                                 _ptr(out_tokens), _ptr(out_count), _ptr(out_accept_prob), ws_ptr, ws_bytes,
+                                 _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_chain")
+    return out_tokens, out_count, out_accept_prob
+
+
+def spec_greedy_accept(target_logits, draft_tokens, *, out_tokens=None, out_count=None, stream=None):
+    """Greedy acceptance for every row.  Returns (out_tokens [B][K+1], out_count [B])."""
+    torch = _torch()
+    _dev(target_logits, "target_logits")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    _dev(draft_tokens, "draft_tokens", torch.int32)
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_count is None:
+        out_count = torch.empty((B,), dtype=torch.int32, device=dev)
+    st = lib().spec_greedy_accept(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft_tokens), B, K, V,
+                                  _ptr(out_tokens), _ptr(out_count), _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_greedy_accept")
+    return out_tokens, out_count
+
+
+def spec_verify_tree(target_logits, draft, node_tokens, parent, temperature, max_depth: int, seed: int,
+                     offset: int, *, draft_kind, out_tokens=None, out_count=None, out_path=None, stream=None):
+    """Tree verify.  target_logits/draft [B][N+1][V], node_tokens/parent int32 [B][N],
+    temperature fp32 [B].  Returns (out_tokens [B][D+1], out_count [B], out_path [B][D])."""
+    torch = _torch()
+    _dev(target_logits, "target_logits")
+    B, N1, V = target_logits.shape
+    N = N1 - 1
+    dk = _kind(draft_kind)
+    _dev(draft, "draft")
+    _dev(node_tokens, "node_tokens", torch.int32)
+    _dev(parent, "parent", torch.int32)
+    _dev(temperature, "temperature", torch.float32)
+    if tuple(draft.shape) != (B, N + 1, V):
+        raise ValueError(f"draft shape {tuple(draft.shape)} != {(B, N + 1, V)}")
+    D = int(max_depth)
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    if out_count is None:
+        out_count = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_path is None:
+        out_path = torch.empty((B, D), dtype=torch.int32, device=dev)
+    st = lib().spec_verify_tree(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), _dtype_code(draft),
+                                dk, _ptr(node_tokens), _ptr(parent), _ptr(temperature), B, N, V, D, int(seed),
+                                int(offset), _ptr(out_tokens), _ptr(out_count), _ptr(out_path), _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_tree")
+    return out_tokens, out_count, out_path

@@ -1,0 +1,150 @@
+// sv_api.cu -- the C ABI declared in include/spec_verify.h: argument checks on the
+// host, launch-shape choice, dispatch to the kernels.  Nothing here allocates.
+#include <cstdlib>
+
+#include "spec_verify.h"
+#include "sv_internal.h"
+
+namespace {
+
+constexpr int kMaxK = 64;
+constexpr int kMaxNodes = 1024;
+constexpr int kMaxDepth = 64;
+constexpr int kMaxV = 1 << 24;
+constexpr int kMaxB = 65535;
+
+struct DeviceInfo {
+    int sms = 0;
+    int major = 0;
+};
+
+// SM count and compute capability of the current device (queried on every call:
+// cheap, and correct when the caller switches devices).
+sv_status device_info(DeviceInfo& info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&info.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        return SV_ERR_CUDA;
+    if (info.major < 10) return SV_ERR_UNSUPPORTED;  // built for sm_103a (thread-block clusters, DSMEM)
+    return SV_OK;
+}
+
+// Launch-shape override for tuning: SPEC_VERIFY_CLUSTER in {1, 2, 4, 8, 16}.
+int cluster_override() {
+    static int v = -1;
+    if (v < 0) {
+        const char* s = std::getenv("SPEC_VERIFY_CLUSTER");
+        int x = s ? std::atoi(s) : 0;
+        v = (x == 1 || x == 2 || x == 4 || x == 8 || x == 16) ? x : 0;
+    }
+    return v;
+}
+
+bool is_dtype(int d) { return d == SV_F32 || d == SV_BF16; }
+
+sv_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return SV_OK;
+    (void)cudaGetLastError();
+    return SV_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace sv {
+
+int choose_cluster(int B, int V, int num_sms) {
+    const int forced = cluster_override();
+    if (forced) return forced;
+    // Spread each row over enough CTAs that the whole grid holds about two CTAs per
+    // SM, but keep at least 2048 elements per CTA and at most 16 CTAs per row.
+    int G = 1;
+    while (G < 16 && (long long)B * G < 2LL * num_sms && V / (2 * G) >= 2048) G *= 2;
+    return G;
+}
+
+}  // namespace sv
+
+extern "C" {
+
+size_t spec_verify_workspace_size(int B, int K, int V) {
+    (void)B;
+    (void)K;
+    (void)V;
+    return 0;
+}
+
+sv_status spec_verify_chain(const void* target_logits, sv_dtype tdt, const void* draft, sv_dtype ddt,
+                            sv_draft_kind dk, const int32_t* draft_tokens, const float* temperature, int B, int K,
+                            int V, uint64_t seed, uint64_t offset, int32_t* out_tokens, int32_t* out_count,
+                            float* out_accept_prob, void* workspace, size_t ws_bytes, void* stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (B < 0 || B > kMaxB || K < 0 || K > kMaxK || V < 1 || V > kMaxV) return SV_ERR_INVALID_ARG;
+    if (!is_dtype(tdt) || !is_dtype(ddt)) return SV_ERR_INVALID_ARG;
+    if (dk != SV_DRAFT_PROBS && dk != SV_DRAFT_LOGITS) return SV_ERR_INVALID_ARG;
+    if (dk == SV_DRAFT_PROBS && ddt != SV_F32) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !temperature || !out_tokens || !out_count || (K > 0 && (!draft_tokens || !draft)))
+        return SV_ERR_INVALID_ARG;
+    DeviceInfo info;
+    sv_status st = device_info(info);
+    if (st != SV_OK) return st;
+    sv::ChainArgs a{target_logits, draft, draft_tokens, temperature, B, K, V, seed, offset,
+                    out_tokens, out_count, out_accept_prob};
+    const int G = sv::choose_cluster(B, V, info.sms);
+    return launch_status(sv::launch_chain(a, tdt, ddt, dk, G, (cudaStream_t)stream));
+}
+
+sv_status spec_greedy_accept(const void* target_logits, sv_dtype tdt, const int32_t* draft_tokens, int B, int K,
+                             int V, int32_t* out_tokens, int32_t* out_count, void* stream) {
+    if (B < 0 || B > kMaxB || K < 0 || K > kMaxK || V < 1 || V > kMaxV) return SV_ERR_INVALID_ARG;
+    if (!is_dtype(tdt)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !out_tokens || !out_count || (K > 0 && !draft_tokens)) return SV_ERR_INVALID_ARG;
+    DeviceInfo info;
+    sv_status st = device_info(info);
+    if (st != SV_OK) return st;
+    sv::ChainArgs a{target_logits, nullptr, draft_tokens, nullptr, B, K, V, 0, 0, out_tokens, out_count, nullptr};
+    const int G = sv::choose_cluster(B, V, info.sms);
+    // the draft kind and dtype do not matter for greedy rows; use the smallest instantiation
+    return launch_status(sv::launch_chain(a, tdt, SV_F32, SV_DRAFT_PROBS, G, (cudaStream_t)stream));
+}
+
+sv_status spec_verify_tree(const void* target_logits, sv_dtype tdt, const void* draft, sv_dtype ddt,
+                           sv_draft_kind dk, const int32_t* node_tokens, const int32_t* parent,
+                           const float* temperature, int B, int N, int V, int max_depth, uint64_t seed,
+                           uint64_t offset, int32_t* out_tokens, int32_t* out_count, int32_t* out_path,
+                           void* stream) {
+    if (B < 0 || B > kMaxB || N < 1 || N > kMaxNodes || V < 1 || V > kMaxV || max_depth < 1 ||
+        max_depth > kMaxDepth)
+        return SV_ERR_INVALID_ARG;
+    if (!is_dtype(tdt) || !is_dtype(ddt)) return SV_ERR_INVALID_ARG;
+    if (dk != SV_DRAFT_PROBS && dk != SV_DRAFT_LOGITS) return SV_ERR_INVALID_ARG;
+    if (dk == SV_DRAFT_PROBS && ddt != SV_F32) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !draft || !node_tokens || !parent || !temperature || !out_tokens || !out_count ||
+        !out_path)
+        return SV_ERR_INVALID_ARG;
+    DeviceInfo info;
+    sv_status st = device_info(info);
+    if (st != SV_OK) return st;
+    sv::TreeArgs a{target_logits, draft, node_tokens, parent, temperature, B, N, V, max_depth, seed, offset,
+                   out_tokens, out_count, out_path};
+    const int G = sv::choose_cluster(B, V, info.sms);
+    return launch_status(sv::launch_tree(a, tdt, ddt, dk, G, (cudaStream_t)stream));
+}
+
+const char* spec_verify_status_string(sv_status status) {
+    switch (status) {
+        case SV_OK: return "SV_OK: success";
+        case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG: a size, pointer, dtype or kind argument is invalid";
+        case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED: outside what this build handles";
+        case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+        case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case SV_ERR_BAD_INPUT: return "SV_ERR_BAD_INPUT: invalid data in a batch row";
+    }
+    return "unknown sv_status";
+}
+
+}  // extern "C"

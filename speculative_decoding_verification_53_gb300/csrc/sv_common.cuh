@@ -1,0 +1,604 @@
+// sv_common.cuh -- device building blocks of the verify kernels (sm_103a).
+//
+// Row statistics for the temperature softmax (online max and sum of exp2),
+// argmax with lowest-index ties, Philox4x64-10 uniforms, thread-block-cluster
+// exchange through distributed shared memory, and the inverse-CDF draw over a
+// vocabulary row that is split across the CTAs of a cluster.
+//
+// The rule these implement is the accept/reject step of speculative decoding
+// ("[논문 리뷰] Fast Inference from Transformers via Speculative Decoding",
+// section 2; "Speculative Decoding and EAGLE", section "정확성 규칙").
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+constexpr int NT = 256;            // threads per CTA
+constexpr int NW = NT / 32;        // warps per CTA
+constexpr int VEC = 8;             // elements per vector step (16 B of bf16, 32 B of fp32)
+constexpr int TILE = 32 * VEC;     // elements per draw tile (one warp, 8 per lane)
+constexpr int UNROLL = 4;          // vector steps in flight per thread
+constexpr int MAX_K = 64;          // chain drafts per row
+constexpr int MAX_NODES = 1024;    // tree nodes per row
+constexpr int MAX_CLUSTER = 16;
+constexpr float LOG2E = 1.4426950408889634f;
+
+enum DTypeCode { DT_F32 = 0, DT_BF16 = 1 };
+enum DraftCode { DK_PROBS = 0, DK_LOGITS = 1 };
+
+// ------------------------------------------------------------------ math
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Maximum that propagates NaN (a NaN anywhere in a row must mark the row invalid).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+__device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
+
+// ---------------------------------------------------------------- Philox
+
+// Philox4x64 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11).  Per round the
+// counter words 0 and 2 are multiplied by the two round constants, the 128-bit
+// products are split, crossed with words 1 and 3 and the key; the key advances
+// by the two Weyl increments between rounds.
+__device__ __forceinline__ void philox4x64_10(uint64_t& x0, uint64_t& x1, uint64_t& x2, uint64_t& x3,
+                                              uint64_t k0, uint64_t k1) {
+    const uint64_t ma = 0xD2E7470EE14C6C93ull, mb = 0xCA5A826395121157ull;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t hi_a = __umul64hi(ma, x0), lo_a = ma * x0;
+        const uint64_t hi_b = __umul64hi(mb, x2), lo_b = mb * x2;
+        const uint64_t y0 = hi_b ^ x1 ^ k0;
+        const uint64_t y2 = hi_a ^ x3 ^ k1;
+        x0 = y0;
+        x1 = lo_b;
+        x2 = y2;
+        x3 = lo_a;
+        k0 += 0x9E3779B97F4A7C15ull;
+        k1 += 0xBB67AE8584CAA73Bull;
+    }
+}
+
+// The two uniforms of one Philox slot: r from word 0 (acceptance), u from word 1 (draw),
+// each (w >> 40) * 2^-24, exactly representable in fp32.
+__device__ __forceinline__ void slot_uniforms(uint64_t seed, uint64_t offset, uint64_t row, uint64_t slot,
+                                              float& r, float& u) {
+    uint64_t x0 = slot, x1 = row, x2 = offset, x3 = 0;
+    philox4x64_10(x0, x1, x2, x3, seed, 0);
+    r = (float)(uint32_t)(x0 >> 40) * (1.0f / 16777216.0f);
+    u = (float)(uint32_t)(x1 >> 40) * (1.0f / 16777216.0f);
+}
+
+// ----------------------------------------------------------------- loads
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <int DT>
+__device__ __forceinline__ float load_one(const void* row, int i) {
+    if (DT == DT_BF16) return __uint_as_float((uint32_t)__ldg((const unsigned short*)row + i) << 16);
+    return __ldg((const float*)row + i);
+}
+
+// Eight consecutive elements e0..e0+7 of a row (e0 a multiple of 8), widened to fp32.
+// Elements at or beyond `hi` read as `pad`.  `al` says the row start is 16-byte aligned.
+template <int DT>
+__device__ __forceinline__ void load8(const void* row, int e0, int hi, bool al, float pad, float x[VEC]) {
+    if (al && e0 + VEC <= hi) {
+        if (DT == DT_BF16) {
+            const uint4 v = ld_nc_v4((const unsigned short*)row + e0);
+            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+        } else {
+            const uint4 a = ld_nc_v4((const float*)row + e0);
+            const uint4 b = ld_nc_v4((const float*)row + e0 + 4);
+            x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+            x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+            x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+            x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) x[j] = (e0 + j < hi) ? load_one<DT>(row, e0 + j) : pad;
+    }
+}
+
+__device__ __forceinline__ float vmax8(const float x[VEC]) {
+    const float a = fmax_nan(fmax_nan(x[0], x[1]), fmax_nan(x[2], x[3]));
+    const float b = fmax_nan(fmax_nan(x[4], x[5]), fmax_nan(x[6], x[7]));
+    return fmax_nan(a, b);
+}
+
+// ------------------------------------------------------ softmax statistics
+
+// Running (max m, sum s of 2^((l - m) * c)) of a set of logits, c = log2(e) / T.
+struct LSE {
+    float m, s;
+    int bad;  // NaN seen
+};
+
+__device__ __forceinline__ void lse_merge(LSE& a, const LSE& b, float c) {
+    a.bad |= b.bad;
+    if (b.m > a.m) {
+        a.s = a.s * ex2((a.m - b.m) * c) + b.s;
+        a.m = b.m;
+    } else if (b.m > neg_inf()) {
+        a.s += b.s * ex2((b.m - a.m) * c);
+    }
+}
+
+__device__ __forceinline__ LSE lse_shfl_xor(const LSE& v, int mask) {
+    LSE o;
+    o.m = __shfl_xor_sync(0xffffffffu, v.m, mask);
+    o.s = __shfl_xor_sync(0xffffffffu, v.s, mask);
+    o.bad = __shfl_xor_sync(0xffffffffu, v.bad, mask);
+    return o;
+}
+
+__device__ __forceinline__ void lse_warp_reduce(LSE& v, float c) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lse_merge(v, lse_shfl_xor(v, o), c);
+}
+
+// One thread's pass over its vector steps of elements [lo, hi) of a row.
+template <int DT>
+__device__ __forceinline__ LSE thread_lse(const void* row, int lo, int hi, bool al, float c) {
+    LSE acc{neg_inf(), 0.f, 0};
+    const int v0 = lo / VEC, v1 = (hi + VEC - 1) / VEC;
+    for (int vb = v0 + (int)threadIdx.x; vb < v1; vb += NT * UNROLL) {
+        float x[UNROLL][VEC];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int v = vb + u * NT;
+            if (v < v1) load8<DT>(row, v * VEC, hi, al, neg_inf(), x[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int v = vb + u * NT;
+            if (v >= v1) break;
+            const float vm = vmax8(x[u]);
+            if (vm != vm) acc.bad = 1;
+            if (vm > acc.m) {
+                acc.s *= ex2((acc.m - vm) * c);
+                acc.m = vm;
+            }
+            if (acc.m > neg_inf()) {
+                float s = 0.f;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) s += ex2((x[u][j] - acc.m) * c);
+                acc.s += s;
+            }
+        }
+    }
+    return acc;
+}
+
+// ----------------------------------------------------------------- argmax
+
+struct ArgMax {
+    float v;
+    int i;
+    int bad;  // NaN seen
+};
+
+__device__ __forceinline__ void argmax_merge(ArgMax& a, const ArgMax& b) {
+    a.bad |= b.bad;
+    if (b.v > a.v || (b.v == a.v && b.i < a.i)) {
+        a.v = b.v;
+        a.i = b.i;
+    }
+}
+
+__device__ __forceinline__ void argmax_warp_reduce(ArgMax& v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ArgMax w;
+        w.v = __shfl_xor_sync(0xffffffffu, v.v, o);
+        w.i = __shfl_xor_sync(0xffffffffu, v.i, o);
+        w.bad = __shfl_xor_sync(0xffffffffu, v.bad, o);
+        argmax_merge(v, w);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ ArgMax thread_argmax(const void* row, int lo, int hi, bool al) {
+    ArgMax acc{neg_inf(), 0x7fffffff, 0};
+    const int v0 = lo / VEC, v1 = (hi + VEC - 1) / VEC;
+    for (int vb = v0 + (int)threadIdx.x; vb < v1; vb += NT * UNROLL) {
+        float x[UNROLL][VEC];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int v = vb + u * NT;
+            if (v < v1) load8<DT>(row, v * VEC, hi, al, neg_inf(), x[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int v = vb + u * NT;
+            if (v >= v1) break;
+            const float vm = vmax8(x[u]);
+            if (vm != vm) acc.bad = 1;
+            if (vm > acc.v) {  // strictly greater: the earlier (lower) index keeps ties
+                int j = 0;
+#pragma unroll
+                for (int t = VEC - 1; t >= 0; --t)
+                    if (x[u][t] == vm) j = t;
+                acc.v = vm;
+                acc.i = v * VEC + j;
+            }
+        }
+    }
+    return acc;
+}
+
+// --------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives and waits (release/acquire on
+// shared::cluster), so DSMEM writes before it are visible after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of `p` (a shared variable of this CTA) in CTA `rank`'s shared memory window.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+    uint32_t local = (uint32_t)__cvta_generic_to_shared(p), remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    return remote;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Per-CTA exchange record published to the cluster (double-buffered by phase).
+struct Xchg {
+    float f[4];
+    int i[4];
+};
+
+// Shared state of a CTA used by the block- and cluster-level reductions.
+struct BlockScratch {
+    Xchg xchg[2];
+    float rf[NW][4];
+    int ri[NW][2];
+    float bf[8];  // broadcast floats
+    int bi[8];    // broadcast ints
+};
+
+// Chunk [lo, hi) of a row owned by CTA g of G: boundaries on multiples of VEC.
+__device__ __forceinline__ void chunk_range(int V, int g, int G, int& lo, int& hi) {
+    const int nvec = (V + VEC - 1) / VEC;
+    lo = (int)(((long long)g * nvec) / G) * VEC;
+    hi = (int)(((long long)(g + 1) * nvec) / G) * VEC;
+    if (hi > V) hi = V;
+    if (lo > V) lo = V;
+}
+
+// Block reduce of up to two LSE pairs, then a cluster-wide combine in rank order.
+// Every thread of every CTA returns the same values.
+__device__ __forceinline__ void cluster_lse2(LSE& a, LSE& b, float c, BlockScratch& sc, int& phase) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    lse_warp_reduce(a, c);
+    lse_warp_reduce(b, c);
+    if (lane == 0) {
+        sc.rf[warp][0] = a.m; sc.rf[warp][1] = a.s;
+        sc.rf[warp][2] = b.m; sc.rf[warp][3] = b.s;
+        sc.ri[warp][0] = a.bad; sc.ri[warp][1] = b.bad;
+    }
+    __syncthreads();
+    Xchg& slot = sc.xchg[phase & 1];
+    if (warp == 0) {
+        LSE x{neg_inf(), 0.f, 0}, y{neg_inf(), 0.f, 0};
+        if (lane < NW) {
+            x = LSE{sc.rf[lane][0], sc.rf[lane][1], sc.ri[lane][0]};
+            y = LSE{sc.rf[lane][2], sc.rf[lane][3], sc.ri[lane][1]};
+        }
+        lse_warp_reduce(x, c);
+        lse_warp_reduce(y, c);
+        if (lane == 0) {
+            slot.f[0] = x.m; slot.f[1] = x.s; slot.f[2] = y.m; slot.f[3] = y.s;
+            slot.i[0] = x.bad; slot.i[1] = y.bad;
+        }
+    }
+    cluster_sync_all();
+    if (warp == 0) {
+        const uint32_t G = cluster_size();
+        LSE x{neg_inf(), 0.f, 0}, y{neg_inf(), 0.f, 0};
+        if ((uint32_t)lane < G) {
+            x.m = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
+            x.s = dsmem_ld_f32(dsmem_addr(&slot.f[1], lane));
+            y.m = dsmem_ld_f32(dsmem_addr(&slot.f[2], lane));
+            y.s = dsmem_ld_f32(dsmem_addr(&slot.f[3], lane));
+            x.bad = dsmem_ld_s32(dsmem_addr(&slot.i[0], lane));
+            y.bad = dsmem_ld_s32(dsmem_addr(&slot.i[1], lane));
+        }
+        lse_warp_reduce(x, c);
+        lse_warp_reduce(y, c);
+        if (lane == 0) {
+            sc.bf[0] = x.m; sc.bf[1] = x.s; sc.bf[2] = y.m; sc.bf[3] = y.s;
+            sc.bi[0] = x.bad; sc.bi[1] = y.bad;
+        }
+    }
+    __syncthreads();
+    a = LSE{sc.bf[0], sc.bf[1], sc.bi[0]};
+    b = LSE{sc.bf[2], sc.bf[3], sc.bi[1]};
+    __syncthreads();
+    ++phase;
+}
+
+__device__ __forceinline__ ArgMax cluster_argmax(ArgMax a, BlockScratch& sc, int& phase) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    argmax_warp_reduce(a);
+    if (lane == 0) {
+        sc.rf[warp][0] = a.v;
+        sc.ri[warp][0] = a.i;
+        sc.ri[warp][1] = a.bad;
+    }
+    __syncthreads();
+    Xchg& slot = sc.xchg[phase & 1];
+    if (warp == 0) {
+        ArgMax x{neg_inf(), 0x7fffffff, 0};
+        if (lane < NW) x = ArgMax{sc.rf[lane][0], sc.ri[lane][0], sc.ri[lane][1]};
+        argmax_warp_reduce(x);
+        if (lane == 0) {
+            slot.f[0] = x.v;
+            slot.i[0] = x.i;
+            slot.i[1] = x.bad;
+        }
+    }
+    cluster_sync_all();
+    if (warp == 0) {
+        const uint32_t G = cluster_size();
+        ArgMax x{neg_inf(), 0x7fffffff, 0};
+        if ((uint32_t)lane < G) {
+            x.v = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
+            x.i = dsmem_ld_s32(dsmem_addr(&slot.i[0], lane));
+            x.bad = dsmem_ld_s32(dsmem_addr(&slot.i[1], lane));
+        }
+        argmax_warp_reduce(x);
+        if (lane == 0) {
+            sc.bf[0] = x.v;
+            sc.bi[0] = x.i;
+            sc.bi[1] = x.bad;
+        }
+    }
+    __syncthreads();
+    ArgMax r{sc.bf[0], sc.bi[0], sc.bi[1]};
+    __syncthreads();
+    ++phase;
+    return r;
+}
+
+// Cluster-wide sum of two floats (fixed order, identical in every CTA).
+__device__ __forceinline__ float2 cluster_sum2(float2 v, BlockScratch& sc, int& phase) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    }
+    if (lane == 0) { sc.rf[warp][0] = v.x; sc.rf[warp][1] = v.y; }
+    __syncthreads();
+    Xchg& slot = sc.xchg[phase & 1];
+    if (warp == 0) {
+        float2 x = make_float2(0.f, 0.f);
+        if (lane < NW) x = make_float2(sc.rf[lane][0], sc.rf[lane][1]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            x.x += __shfl_xor_sync(0xffffffffu, x.x, o);
+            x.y += __shfl_xor_sync(0xffffffffu, x.y, o);
+        }
+        if (lane == 0) { slot.f[0] = x.x; slot.f[1] = x.y; }
+    }
+    cluster_sync_all();
+    if (warp == 0) {
+        const uint32_t G = cluster_size();
+        float2 x = make_float2(0.f, 0.f);
+        if ((uint32_t)lane < G) {
+            x.x = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
+            x.y = dsmem_ld_f32(dsmem_addr(&slot.f[1], lane));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            x.x += __shfl_xor_sync(0xffffffffu, x.x, o);
+            x.y += __shfl_xor_sync(0xffffffffu, x.y, o);
+        }
+        if (lane == 0) { sc.bf[0] = x.x; sc.bf[1] = x.y; }
+    }
+    __syncthreads();
+    float2 r = make_float2(sc.bf[0], sc.bf[1]);
+    __syncthreads();
+    ++phase;
+    return r;
+}
+
+// ------------------------------------------------------------------ draw
+
+// Inverse-CDF draw over a row split across the cluster: the token is the smallest
+// index i whose prefix sum of weights exceeds u * Z (Z the row's total weight).
+// The weight functor WF provides eval8(e0, hi, w[8]) for elements e0..e0+7 (0 beyond hi).
+//
+// Pass 1: per-tile sums (tile = 256 elements, one warp) into shared memory, CTA
+// totals exchanged across the cluster.  Pass 2: the CTA whose prefix range holds
+// u * Z narrows it to a tile, a lane and an element.  Where rounding leaves the
+// target past the last element of a range, the last element with non-zero weight
+// in that range is taken.
+//
+// Returns in *out_token the token (valid in the owner CTA) and the owner rank;
+// returns false (no owner) when the total weight is zero.
+struct DrawResult {
+    int owner;
+    int token;
+    float Z;
+};
+
+template <class WF>
+__device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float* tile_sum, BlockScratch& sc,
+                                   int& phase) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ntiles = (hi - lo + TILE - 1) / TILE;
+    for (int t = warp; t < ntiles; t += NW) {
+        float w[VEC];
+        wf.eval8(lo + t * TILE + lane * VEC, hi, w);
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) s += w[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) tile_sum[t] = s;
+    }
+    __syncthreads();
+    Xchg& slot = sc.xchg[phase & 1];
+    if (warp == 0) {
+        float z = 0.f;
+        for (int t = lane; t < ntiles; t += 32) z += tile_sum[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (lane == 0) slot.f[0] = z;
+    }
+    cluster_sync_all();
+    if (warp == 0) {
+        const uint32_t G = cluster_size();
+        float z = 0.f;
+        if ((uint32_t)lane < G) z = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
+        float incl = z;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        const float Z = __shfl_sync(0xffffffffu, incl, 31);
+        const float t = u * Z;
+        const unsigned hit = __ballot_sync(0xffffffffu, (uint32_t)lane < G && incl > t);
+        const unsigned nz = __ballot_sync(0xffffffffu, (uint32_t)lane < G && z > 0.f);
+        int owner = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : -1);
+        const float excl = __shfl_sync(0xffffffffu, incl - z, owner < 0 ? 0 : owner);
+        if (lane == 0) {
+            sc.bi[0] = (Z > 0.f) ? owner : -1;
+            sc.bi[1] = hit ? 0 : 1;  // 1: take the last non-zero element of the owner
+            sc.bf[0] = t - excl;
+            sc.bf[1] = Z;
+        }
+    }
+    __syncthreads();
+    DrawResult res{sc.bi[0], -1, sc.bf[1]};
+    const bool take_last = sc.bi[1] != 0;
+    const float t_loc = sc.bf[0];
+    __syncthreads();
+    ++phase;
+    if (res.owner < 0 || (uint32_t)res.owner != cluster_rank()) return res;
+    // ---- owner CTA: warp 0 narrows the target to a tile, a lane and an element
+    if (warp == 0) {
+        int tile = -1, last_nz_tile = -1;
+        float t_tile = 0.f;
+        float cum = 0.f;
+        for (int base = 0; base < ntiles && tile < 0; base += 32) {
+            const float v = (base + lane < ntiles) ? tile_sum[base + lane] : 0.f;
+            float incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            const unsigned nzb = __ballot_sync(0xffffffffu, v > 0.f);
+            if (nzb) last_nz_tile = base + 31 - __clz(nzb);
+            const unsigned h = take_last ? 0u : __ballot_sync(0xffffffffu, cum + incl > t_loc);
+            if (h) {
+                const int f = __ffs(h) - 1;
+                tile = base + f;
+                t_tile = t_loc - (cum + __shfl_sync(0xffffffffu, incl - v, f));
+            }
+            cum += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        bool last_mode = take_last;
+        if (tile < 0) {
+            tile = last_nz_tile;
+            last_mode = true;
+        }
+        int token = -1;
+        if (tile >= 0) {
+            const int e0 = lo + tile * TILE + lane * VEC;
+            float w[VEC];
+            wf.eval8(e0, hi, w);
+            float ls = 0.f;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) ls += w[j];
+            float incl = ls;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            const unsigned h = last_mode ? 0u : __ballot_sync(0xffffffffu, incl > t_tile);
+            const unsigned nzl = __ballot_sync(0xffffffffu, ls > 0.f);
+            int f;
+            bool lane_last = last_mode;
+            if (h) {
+                f = __ffs(h) - 1;
+            } else {
+                f = nzl ? 31 - __clz(nzl) : 0;
+                lane_last = true;
+            }
+            const float t_lane = t_tile - __shfl_sync(0xffffffffu, incl - ls, f);
+            if (lane == f) {
+                int pick = -1, last_nz = -1;
+                float run = 0.f;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    if (w[j] > 0.f) last_nz = j;
+                    run += w[j];
+                    if (!lane_last && pick < 0 && run > t_lane) pick = j;
+                }
+                if (pick < 0) pick = last_nz < 0 ? 0 : last_nz;
+                token = e0 + pick;
+            }
+            token = __shfl_sync(0xffffffffu, token, f);
+        }
+        if (lane == 0) sc.bi[2] = token;
+    }
+    __syncthreads();
+    res.token = sc.bi[2];
+    __syncthreads();
+    return res;
+}
+
+}  // namespace sv

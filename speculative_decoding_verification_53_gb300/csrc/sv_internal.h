@@ -1,0 +1,45 @@
+// sv_internal.h -- argument blocks and launchers shared by the host entry points
+// (sv_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+struct ChainArgs {
+    const void* target;        // [B][K+1][V]
+    const void* draft;         // [B][K][V] probs (fp32) or logits
+    const int32_t* tokens;     // [B][K]
+    const float* temperature;  // [B]; nullptr: every row greedy
+    int B, K, V;
+    uint64_t seed, offset;
+    int32_t* out_tokens;       // [B][K+1]
+    int32_t* out_count;        // [B]
+    float* out_accept_prob;    // [B][K] or nullptr
+};
+
+struct TreeArgs {
+    const void* target;        // [B][N+1][V]
+    const void* draft;         // [B][N+1][V]
+    const int32_t* node_tokens;
+    const int32_t* parent;
+    const float* temperature;
+    int B, N, V, max_depth;
+    uint64_t seed, offset;
+    int32_t* out_tokens;       // [B][D+1]
+    int32_t* out_count;        // [B]
+    int32_t* out_path;         // [B][D]
+};
+
+// Cluster size (CTAs per batch row) for a launch over B batch rows.
+int choose_cluster(int B, int V, int num_sms);
+
+cudaError_t launch_chain(const ChainArgs& a, int tdt, int ddt, int dk, int cluster, cudaStream_t stream);
+cudaError_t launch_tree(const TreeArgs& a, int tdt, int ddt, int dk, int cluster, cudaStream_t stream);
+
+// Dynamic shared memory (tile sums of the draw) for a row split `cluster` ways.
+size_t draw_smem_bytes(int V, int cluster);
+
+}  // namespace sv

@@ -258,3 +258,20 @@ def chain_as_tree(w: dict) -> dict:
     return dict(kind="tree", target=target, draft=np.concatenate([draft, pad], axis=1),
                 draft_kind=w["draft_kind"], node_tokens=w["tokens"].copy(), parent=parent,
                 temperature=w["temperature"].copy(), max_depth=K, seed=w["seed"], offset=w["offset"])
+
+
+def redraw_tokens(w: dict, temperature: float, seed: int) -> dict:
+    """The same chain logits with drafted tokens (and temperatures) redrawn for another
+    temperature; row b draws from ``default_rng([seed, b, 1])``."""
+    B, K = w["tokens"].shape
+    tokens = np.empty_like(w["tokens"])
+    for b in range(B):
+        rng = np.random.default_rng([seed, b, 1])
+        if w["draft_kind"] == DRAFT_PROBS:
+            tokens[b] = draft_tokens_from_probs(rng, w["draft"][b])
+        else:
+            tokens[b] = draft_tokens_from_logits(rng, as_f32(w["draft"][b]), temperature)
+    out = dict(w)
+    out["tokens"] = tokens
+    out["temperature"] = np.full(B, temperature, np.float32)
+    return out

@@ -1,0 +1,89 @@
+"""The C-ABI library builds, loads and exports every symbol include/*.h declares;
+host-side argument checks answer without launching anything (no GPU needed)."""
+import ctypes
+import glob
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names |= set(re.findall(r"^SV_API\s+[^;(]*?\b(\w+)\s*\(", text, re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from speculative_decoding_verification_53_gb300 import build
+    build.build()
+    import speculative_decoding_verification_53_gb300 as sv
+    return sv.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_symbols()
+    assert {"spec_verify_chain", "spec_verify_tree", "spec_greedy_accept", "spec_verify_workspace_size",
+            "spec_verify_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    path = lib._name
+    for name in _declared_symbols():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported by {path}"
+
+
+def test_only_the_c_abi_is_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    exported = {e for e in exported if not e.startswith("_")}
+    assert exported == _declared_symbols()
+
+
+def test_status_strings(lib):
+    import speculative_decoding_verification_53_gb300 as sv
+    for code in range(6):
+        assert sv.spec_verify_status_string(code).startswith("SV_")
+    assert "unknown" in sv.spec_verify_status_string(99)
+
+
+def test_argument_errors_are_reported_before_any_launch(lib):
+    import speculative_decoding_verification_53_gb300 as sv
+    vp = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    ch = lib.spec_verify_chain
+    # negative B, K too large, V = 0, bad dtype, probs with a bf16 draft dtype
+    assert ch(vp, 0, vp, 0, 0, vp, vp, -1, 4, 100, 0, 0, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert ch(vp, 0, vp, 0, 0, vp, vp, 1, 65, 100, 0, 0, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert ch(vp, 0, vp, 0, 0, vp, vp, 1, 4, 0, 0, 0, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert ch(vp, 7, vp, 0, 0, vp, vp, 1, 4, 100, 0, 0, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert ch(vp, 0, vp, 1, 0, vp, vp, 1, 4, 100, 0, 0, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert ch(None, 0, vp, 0, 0, vp, vp, 1, 4, 100, 0, 0, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    # an empty batch is a successful no-op
+    assert ch(None, 0, None, 0, 0, None, None, 0, 4, 100, 0, 0, None, None, None, None, 0, None) == sv.SV_OK
+    g = lib.spec_greedy_accept
+    assert g(vp, 0, vp, 1, -1, 100, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    assert g(vp, 0, None, 1, 3, 100, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    t = lib.spec_verify_tree
+    # N = 0, depth 0, depth 65, N over the limit, missing parent array
+    assert t(vp, 0, vp, 0, 1, vp, vp, vp, 1, 0, 100, 4, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    assert t(vp, 0, vp, 0, 1, vp, vp, vp, 1, 8, 100, 0, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    assert t(vp, 0, vp, 0, 1, vp, vp, vp, 1, 8, 100, 65, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    assert t(vp, 0, vp, 0, 1, vp, vp, vp, 1, 1025, 100, 4, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    assert t(vp, 0, vp, 0, 1, vp, None, vp, 1, 8, 100, 4, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+
+
+def test_binding_refuses_to_run_without_the_library(monkeypatch, tmp_path):
+    import speculative_decoding_verification_53_gb300 as sv
+    monkeypatch.setattr(sv, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(sv, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        sv.lib()
