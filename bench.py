@@ -1,0 +1,524 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-decoding verify step on GB300.
+
+Default workload (the headline metric): single-stream chain verify, B=1, K=5,
+V=128256, T=0.8, bf16 target logits, fp32 draft probabilities.  One step is one
+verify round (the whole path: softmax statistics, acceptance, first rejection,
+replacement or bonus draw) of one batch.  ROUNDS distinct rounds (default 64,
+about 262 MB, more than the 129 MB L2) stay resident in HBM and the steps cycle
+through them; steps are replayed from CUDA graphs so that host launch gaps do
+not enter the device timing.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload single_stream|large_batch|mixed_batch|tree]
+
+Prints one JSON line (rank 0).  `value` is verify rows/s over all ranks;
+`roofline` relates the kernel's algorithmic bytes per launch (the rows the rule
+needs: target rows up to the first rejection, gathered draft entries, the draft
+row of the rejected position) to its event-timed duration; `e2e` is the same
+metric through the public API with host buffers (copies inside the timed
+region); `cpu_baseline` is the fp64 oracle on a bounded sample, single thread.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify rows/s and achieved HBM GB/s vs GB300 peak at V=128256, K=5"
+UNIT = "verify rows/s"
+FALLBACK_HBM_GBS = 6800.0
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+# ------------------------------------------------------------------ inputs
+
+def make_workload(name: str, rank: int, rounds: int, batch: int = 0):
+    from speculative_decoding_verification_53_gb300 import synth
+    seed = 1000 + rank
+    if name == "single_stream":
+        w = synth.single_stream(seed=seed, B=rounds)  # row r = round r (B=1 per step)
+        return dict(w, per_step_rows=1, desc="single-stream chain verify B=1 K=5 V=128256 T=0.8, "
+                                             "bf16 target logits, fp32 draft probabilities")
+    if name == "large_batch":
+        B = batch or 256
+        w = synth.large_batch(seed=seed, temperature=0.7, sigma=1.0, B=B)
+        return dict(w, per_step_rows=B, desc=f"large-batch chain verify B={B} K=8 V=152064 T=0.7, "
+                                             "bf16 target and draft logits, draft noise sigma=1")
+    if name == "mixed_batch":
+        w = synth.mixed_batch(seed=seed)
+        return dict(w, per_step_rows=64, desc="mixed greedy/sampling chain verify B=64 K=5 V=32000, bf16 logits")
+    if name == "tree":
+        w = synth.tree(seed=seed, temperature=1.0)
+        return dict(w, per_step_rows=16, desc="tree verify B=16 N=60 depth<=6 V=128256 T=1, bf16 logits")
+    raise ValueError(name)
+
+
+def to_dev(a, device):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def pinned(a):
+    import torch
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+    return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
+
+
+# ----------------------------------------------------------------- helpers
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_53_gb300", "csrc")
+    for d in (pkg, os.path.join(ROOT, "include")):
+        for f in sorted(os.listdir(d)):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        if j.get("hbm_gbs"):
+            return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per launch of the timed kernel from the committed ncu summary, if the
+    kernel sources still hash to the value recorded there (else None)."""
+    path = os.path.join(ROOT, "profiles", f"chain_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None, None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    hm = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    if not m or not hm or hm.group(1) != kernel_source_hash():
+        return None, path
+    return float(m.group(1)), path
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_bytes_chain(w, rows, counts):
+    """Bytes the rule needs for the given rounds: target rows 0..j, the gathered draft
+    entries (probabilities) or draft rows 0..min(j, K-1) (logits), the draft row of a
+    rejected position, tokens, temperature and the outputs.  j = count - 1."""
+    target, draft = w["target"], w["draft"]
+    _, K1, V = target.shape
+    K = K1 - 1
+    tb = V * target.dtype.itemsize
+    db = V * draft.dtype.itemsize
+    total = 0
+    for b, cnt in zip(rows, counts):
+        j = int(cnt) - 1
+        greedy = not (w["temperature"][b] > 0)
+        total += (j + 1) * tb + K * 4 + 4 + (K + 1) * 4 + 4
+        if greedy:
+            continue
+        evaluated = min(j, K - 1) + 1 if K > 0 else 0
+        if w["draft_kind"] == 0:  # probabilities: gathered entries, plus the rejected row
+            total += evaluated * 4 + (db if j < K else 0)
+        else:  # logits: every evaluated draft row is streamed for its statistics
+            total += evaluated * db
+    return total
+
+
+def algorithmic_bytes_tree(w, counts, paths):
+    target = w["target"]
+    B, N1, V = target.shape
+    tb = V * target.dtype.itemsize
+    db = V * w["draft"].dtype.itemsize
+    total = 0
+    for b in range(B):
+        visited = int(counts[b])  # root plus accepted nodes: one row each
+        total += visited * tb + N1 * 8 + 4 + 4
+        if w["temperature"][b] > 0:
+            par = w["parent"][b]
+            nodes = [-1] + [int(x) for x in paths[b][: visited - 1]]
+            total += sum(db for n in nodes if (par == n).any())
+    return total
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, device):
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    from speculative_decoding_verification_53_gb300 import build as svbuild
+
+    if rank == 0:
+        svbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    sv.lib()
+    w = make_workload(args.workload, rank, args.rounds, args.batch)
+    tree = w["kind"] == "tree"
+    per_step_rows = w["per_step_rows"]
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+
+    dt = to_dev(w["target"], device)
+    dd = to_dev(w["draft"], device)
+    if tree:
+        dtok, dpar = to_dev(w["node_tokens"], device), to_dev(w["parent"], device)
+    else:
+        dtok = to_dev(w["tokens"], device)
+    dtemp = to_dev(w["temperature"], device)
+    kind = "probs" if w["draft_kind"] == 0 else "logits"
+    n_inputs = dt.shape[0] // per_step_rows  # distinct resident input sets
+
+    chunk = min(args.steps, 1000)
+    K_ = w["tokens"].shape[1] if not tree else None
+    if tree:
+        D = w["max_depth"]
+        out_t = torch.empty((chunk, per_step_rows, D + 1), dtype=torch.int32, device=device)
+        out_c = torch.empty((chunk, per_step_rows), dtype=torch.int32, device=device)
+        out_p = torch.empty((chunk, per_step_rows, D), dtype=torch.int32, device=device)
+    else:
+        out_t = torch.empty((chunk, per_step_rows, K_ + 1), dtype=torch.int32, device=device)
+        out_c = torch.empty((chunk, per_step_rows), dtype=torch.int32, device=device)
+
+    def step(i, slot):
+        r = (i % n_inputs) * per_step_rows
+        sl = slice(r, r + per_step_rows)
+        if tree:
+            sv.spec_verify_tree(dt[sl], dd[sl], dtok[sl], dpar[sl], dtemp[sl], D, 17, i, draft_kind=kind,
+                                out_tokens=out_t[slot], out_count=out_c[slot], out_path=out_p[slot])
+        else:
+            sv.spec_verify_chain(dt[sl], dd[sl], dtok[sl], dtemp[sl], 17, i, draft_kind=kind,
+                                 out_tokens=out_t[slot], out_count=out_c[slot])
+
+    for i in range(max(args.warmup, 3)):
+        step(i, i % chunk)
+    torch.cuda.synchronize(device)
+
+    def capture(nsteps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nsteps):
+                step(i, i)
+        return g
+
+    reps, rem = divmod(args.steps, chunk)
+    g_main = capture(chunk) if reps else None
+    g_rem = capture(rem) if rem else None
+    for g in (g_main, g_rem):
+        if g is not None:
+            g.replay()
+    torch.cuda.synchronize(device)
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        t_wall = time.time()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+        start.record(stream)
+        for _ in range(reps):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        if world > 1:
+            torch.distributed.barrier()
+        elapsed_ms = start.elapsed_time(end)
+        # keep the GPU busy (untimed) so that the clock sampler sees at least ~1.5 s of load
+        while time.time() - t_wall < 1.5 and g_main is not None:
+            g_main.replay()
+            torch.cuda.synchronize(device)
+    clock = clocks.summary()
+
+    # per-step algorithmic bytes of the captured steps (read back their outputs)
+    steps_in_chunk = chunk if reps else rem
+    counts = out_c[:steps_in_chunk].cpu().numpy()
+    if tree:
+        paths = out_p[:steps_in_chunk].cpu().numpy()
+        bytes_steps = [algorithmic_bytes_tree(w, counts[s], paths[s]) for s in range(steps_in_chunk)]
+    else:
+        bytes_steps = []
+        for s in range(steps_in_chunk):
+            r = (s % n_inputs) * per_step_rows
+            bytes_steps.append(algorithmic_bytes_chain(w, range(r, r + per_step_rows), counts[s]))
+    bytes_per_launch = float(np.mean(bytes_steps))
+    mean_count = float(counts.mean())
+
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    max_ms = float(t.item())
+    ms_per_step = max_ms / args.steps
+    rows_total = per_step_rows * args.steps * world
+    value = rows_total / (max_ms / 1e3)
+
+    # end to end: host buffers, copies inside the timed region, through the public API
+    e2e = run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind)
+
+    cpu = run_cpu_baseline(w, per_step_rows, n_inputs, tree) if (rank == 0 and not args.no_cpu_baseline) else None
+    if rank != 0:
+        return None
+    peak, peak_src = measured_peak()
+    achieved = bytes_per_launch / (ms_per_step / 1e3) / 1e9
+    traffic, prof = profile_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w["desc"], "batch_rows_per_step": per_step_rows,
+                   "resident_input_sets": n_inputs,
+                   "resident_bytes": int(dt.numel() * dt.element_size() + dd.numel() * dd.element_size()),
+                   "l2": "inputs larger than L2 (resident sets cycled, no flush)",
+                   "timing": "CUDA-graph replay, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}", "mean_tokens_per_round": mean_count},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (STREAM copy)",
+                     "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "kernel": "tree_kernel" if tree else "chain_kernel",
+                     "traffic_source": prof},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps,
+        "clocks": clock,
+    }
+    return line
+
+
+def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    n = min(args.e2e_steps, max(args.steps, 3))
+    sl = slice(0, per_step_rows)
+    ht, hd = pinned(w["target"][sl]), pinned(w["draft"][sl])
+    htemp = pinned(w["temperature"][sl])
+    dt = torch.empty(ht.shape, dtype=ht.dtype, device=device)
+    dd = torch.empty(hd.shape, dtype=hd.dtype, device=device)
+    dtemp = torch.empty(htemp.shape, dtype=htemp.dtype, device=device)
+    if tree:
+        htok, hpar = pinned(w["node_tokens"][sl]), pinned(w["parent"][sl])
+        dtok = torch.empty(htok.shape, dtype=torch.int32, device=device)
+        dpar = torch.empty(hpar.shape, dtype=torch.int32, device=device)
+        D = w["max_depth"]
+        ho_t = torch.empty((per_step_rows, D + 1), dtype=torch.int32).pin_memory()
+    else:
+        htok = pinned(w["tokens"][sl])
+        dtok = torch.empty(htok.shape, dtype=torch.int32, device=device)
+        ho_t = torch.empty((per_step_rows, htok.shape[1] + 1), dtype=torch.int32).pin_memory()
+    ho_c = torch.empty((per_step_rows,), dtype=torch.int32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in ([ht, hd, htok, htemp] + ([hpar] if tree else [])))
+    d2h = ho_t.numel() * 4 + ho_c.numel() * 4
+
+    def one(i):
+        dt.copy_(ht, non_blocking=True)
+        dd.copy_(hd, non_blocking=True)
+        dtok.copy_(htok, non_blocking=True)
+        dtemp.copy_(htemp, non_blocking=True)
+        if tree:
+            dpar.copy_(hpar, non_blocking=True)
+            ot, oc, _ = sv.spec_verify_tree(dt, dd, dtok, dpar, dtemp, D, 23, i, draft_kind=kind)
+        else:
+            ot, oc, _ = sv.spec_verify_chain(dt, dd, dtok, dtemp, 23, i, draft_kind=kind)
+        ho_t.copy_(ot, non_blocking=True)
+        ho_c.copy_(oc, non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(n):
+        one(i)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    ms = start.elapsed_time(end)
+    return {"value": per_step_rows * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": ms / n}
+
+
+def run_cpu_baseline(w, per_step_rows, n_inputs, tree, budget_s=10.0):
+    """The oracle (fp64, one thread, unmodified) on a bounded sample of the same workload."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    done = 0
+    i = 0
+    while time.perf_counter() - t0 < budget_s:
+        r = (i % n_inputs) * per_step_rows
+        sl = slice(r, r + per_step_rows)
+        if tree:
+            oracle.verify_tree(w["target"][sl], w["draft"][sl], w["node_tokens"][sl], w["parent"][sl],
+                               w["temperature"][sl], w["max_depth"], 17, i, draft_kind=w["draft_kind"])
+        else:
+            oracle.verify_chain(w["target"][sl], w["draft"][sl], w["tokens"][sl], w["temperature"][sl], 17, i,
+                                draft_kind=w["draft_kind"])
+        done += per_step_rows
+        i += 1
+    el = time.perf_counter() - t0
+    return {"value": done / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{i} steps ({done} verify rows) of the same workload in {el:.1f} s, single thread, fp64"}
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args, rank):
+    """The oracle as it stands, timed on the host cores, on the same workload, metric and unit."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = make_workload(args.workload, 0, args.rounds, args.batch)
+    per_step_rows = w["per_step_rows"]
+    n_inputs = w["target"].shape[0] // per_step_rows
+    tree = w["kind"] == "tree"
+    budget = 120.0
+
+    def one(i):
+        r = (i % n_inputs) * per_step_rows
+        sl = slice(r, r + per_step_rows)
+        if tree:
+            oracle.verify_tree(w["target"][sl], w["draft"][sl], w["node_tokens"][sl], w["parent"][sl],
+                               w["temperature"][sl], w["max_depth"], 17, i, draft_kind=w["draft_kind"])
+        else:
+            oracle.verify_chain(w["target"][sl], w["draft"][sl], w["tokens"][sl], w["temperature"][sl], 17, i,
+                                draft_kind=w["draft_kind"])
+
+    for i in range(max(args.warmup, 3)):
+        one(i)
+        if i >= 3 and args.warmup > 3:
+            break
+    t0 = time.perf_counter()
+    done = 0
+    while done < args.steps and (time.perf_counter() - t0) < budget:
+        one(done)
+        done += 1
+    el = time.perf_counter() - t0
+    value = done * per_step_rows / el
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": done,
+            "warmup": max(args.warmup, 3), "ms_per_step": el / max(done, 1) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w["desc"], "batch_rows_per_step": per_step_rows,
+                       "steps_requested": args.steps, "time_budget_s": budget},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{done} steps of the workload on one host core (fp64 C oracle)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# -------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="single_stream",
+                    choices=["single_stream", "large_batch", "mixed_batch", "tree"])
+    ap.add_argument("--rounds", type=int, default=64, help="resident rounds of the single-stream workload")
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--batch", type=int, default=0, help="batch rows of the large-batch workload (default 256)")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    line = run_ours(args, rank, world, device)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

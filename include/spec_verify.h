@@ -161,6 +161,10 @@ SV_API sv_status spec_verify_tree(const void *target_logits, sv_dtype tdt,
 /* Static, NUL-terminated description of a status code. */
 SV_API const char *spec_verify_status_string(sv_status status);
 
+/* Description of the CUDA error behind the most recent SV_ERR_CUDA returned on the
+ * calling thread ("no CUDA error" if there was none).  Static storage; not freed. */
+SV_API const char *spec_verify_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,7 @@ SV_F32, SV_BF16 = 0, 1
 SV_DRAFT_PROBS, SV_DRAFT_LOGITS = 0, 1
 
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_chain", "spec_greedy_accept", "spec_verify_tree",
-           "spec_verify_status_string")
+           "spec_verify_status_string", "spec_verify_last_cuda_error")
 
 _lib = None
 
@@ -33,7 +33,8 @@ class SpecVerifyError(RuntimeError):
 
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {spec_verify_status_string(status)}")
+        detail = f" ({lib().spec_verify_last_cuda_error().decode()})" if status == SV_ERR_CUDA else ""
+        super().__init__(f"{where}: {spec_verify_status_string(status)}{detail}")
 
 
 def lib() -> ctypes.CDLL:
@@ -56,6 +57,8 @@ def lib() -> ctypes.CDLL:
     L.spec_verify_tree.restype = ci
     L.spec_verify_status_string.argtypes = [ci]
     L.spec_verify_status_string.restype = ctypes.c_char_p
+    L.spec_verify_last_cuda_error.argtypes = []
+    L.spec_verify_last_cuda_error.restype = ctypes.c_char_p
     _lib = L
     return L
 

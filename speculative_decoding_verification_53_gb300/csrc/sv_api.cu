@@ -13,23 +13,6 @@ constexpr int kMaxDepth = 64;
 constexpr int kMaxV = 1 << 24;
 constexpr int kMaxB = 65535;
 
-struct DeviceInfo {
-    int sms = 0;
-    int major = 0;
-};
-
-// SM count and compute capability of the current device (queried on every call:
-// cheap, and correct when the caller switches devices).
-sv_status device_info(DeviceInfo& info) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SV_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&info.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
-        return SV_ERR_CUDA;
-    if (info.major < 10) return SV_ERR_UNSUPPORTED;  // built for sm_103a (thread-block clusters, DSMEM)
-    return SV_OK;
-}
-
 // Launch-shape override for tuning: SPEC_VERIFY_CLUSTER in {1, 2, 4, 8, 16}.
 int cluster_override() {
     static int v = -1;
@@ -43,11 +26,90 @@ int cluster_override() {
 
 bool is_dtype(int d) { return d == SV_F32 || d == SV_BF16; }
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 sv_status launch_status(cudaError_t e) {
     if (e == cudaSuccess) return SV_OK;
+    g_last_cuda_error = e;
     (void)cudaGetLastError();
     return SV_ERR_CUDA;
 }
+
+struct DeviceInfo {
+    int sms = 0;
+    int major = 0;
+};
+
+// SM count and compute capability of the current device (queried on every call:
+// cheap, and correct when the caller switches devices).
+sv_status device_info(DeviceInfo& info) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&info.major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return launch_status(e);
+    if (info.major < 10) return SV_ERR_UNSUPPORTED;  // built for sm_103a (thread-block clusters, DSMEM)
+    return SV_OK;
+}
+
+// SPEC_VERIFY_NO_STAGING=1 forces the register-streaming kernels (for comparison runs).
+bool staging_disabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* s = std::getenv("SPEC_VERIFY_NO_STAGING");
+        v = (s && s[0] == '1') ? 1 : 0;
+    }
+    return v == 1;
+}
+
+size_t dtype_size(int d) { return d == SV_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t round16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+// Staging layout for a chain launch, or nslot = 0 when the staged kernel does not apply
+// (rows not 16-byte aligned, or one slot does not fit in shared memory).
+sv::StageLayout chain_stage_layout(const void* target, int tdt, const void* draft, int ddt, int dk, bool uses_draft,
+                                   int B, int K, int V, int G, int num_sms) {
+    sv::StageLayout L{0, 0, 0, 0, 0};
+    const size_t tsz = dtype_size(tdt), dsz = dk == SV_DRAFT_PROBS ? 4 : dtype_size(ddt);
+    if (!aligned16(target) || (V * tsz) % 16) return L;
+    if (uses_draft && (!aligned16(draft) || (V * dsz) % 16)) return L;
+    const size_t nvec = (V + 7) / 8, cmax = ((nvec + G - 1) / G) * 8;
+    const size_t t_bytes = round16(cmax * tsz);
+    const size_t d_bytes = (uses_draft && dk == SV_DRAFT_LOGITS) ? round16(cmax * dsz) : 0;
+    const size_t probs = (uses_draft && dk == SV_DRAFT_PROBS) ? round16(cmax * 4) : 0;
+    const size_t fixed = sv::STAGE_HEADER + probs + sv::draw_smem_bytes(V, G) + 64;
+    const bool small = (long long)B * G <= num_sms;  // one CTA per SM or fewer: prefetch positions ahead
+    const size_t budget = small ? (size_t)sv::MAX_DYN_SMEM - 8192 : (size_t)100 * 1024;
+    const size_t slot = t_bytes + d_bytes;
+    if (fixed + slot > budget) return L;
+    size_t nslot = small ? (budget - fixed) / slot : 1;
+    if (nslot > (size_t)K + 1) nslot = K + 1;
+    if (nslot > 16) nslot = 16;
+    L.nslot = (int)nslot;
+    L.slot_bytes = (int)slot;
+    L.t_bytes = (int)t_bytes;
+    L.probs_bytes = (int)probs;
+    L.prefetch_l2 = small ? 1 : 0;
+    return L;
+}
+
+// Staged kernel when it applies, else the register-streaming kernel.
+sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_draft, int num_sms,
+                    cudaStream_t stream) {
+    const int G = sv::choose_cluster(a.B, a.V, num_sms);
+    const sv::StageLayout L = chain_stage_layout(a.target, tdt, a.draft, ddt, dk, uses_draft, a.B, a.K, a.V, G, num_sms);
+    if (L.nslot > 0 && !staging_disabled()) {
+        const cudaError_t e = sv::launch_chain_staged(a, L, tdt, ddt, dk, G, stream);
+        if (e == cudaSuccess) return SV_OK;
+        if (e != cudaErrorInvalidClusterSize) return launch_status(e);
+        (void)cudaGetLastError();
+    }
+    return launch_status(sv::launch_chain(a, tdt, ddt, dk, G, stream));
+}
+
 
 }  // namespace
 
@@ -92,8 +154,7 @@ sv_status spec_verify_chain(const void* target_logits, sv_dtype tdt, const void*
     if (st != SV_OK) return st;
     sv::ChainArgs a{target_logits, draft, draft_tokens, temperature, B, K, V, seed, offset,
                     out_tokens, out_count, out_accept_prob};
-    const int G = sv::choose_cluster(B, V, info.sms);
-    return launch_status(sv::launch_chain(a, tdt, ddt, dk, G, (cudaStream_t)stream));
+    return run_chain(a, tdt, ddt, dk, K > 0, info.sms, (cudaStream_t)stream);
 }
 
 sv_status spec_greedy_accept(const void* target_logits, sv_dtype tdt, const int32_t* draft_tokens, int B, int K,
@@ -106,9 +167,8 @@ sv_status spec_greedy_accept(const void* target_logits, sv_dtype tdt, const int3
     sv_status st = device_info(info);
     if (st != SV_OK) return st;
     sv::ChainArgs a{target_logits, nullptr, draft_tokens, nullptr, B, K, V, 0, 0, out_tokens, out_count, nullptr};
-    const int G = sv::choose_cluster(B, V, info.sms);
     // the draft kind and dtype do not matter for greedy rows; use the smallest instantiation
-    return launch_status(sv::launch_chain(a, tdt, SV_F32, SV_DRAFT_PROBS, G, (cudaStream_t)stream));
+    return run_chain(a, tdt, SV_F32, SV_DRAFT_PROBS, false, info.sms, (cudaStream_t)stream);
 }
 
 sv_status spec_verify_tree(const void* target_logits, sv_dtype tdt, const void* draft, sv_dtype ddt,
@@ -133,6 +193,10 @@ sv_status spec_verify_tree(const void* target_logits, sv_dtype tdt, const void* 
                    out_tokens, out_count, out_path};
     const int G = sv::choose_cluster(B, V, info.sms);
     return launch_status(sv::launch_tree(a, tdt, ddt, dk, G, (cudaStream_t)stream));
+}
+
+const char* spec_verify_last_cuda_error(void) {
+    return g_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda_error);
 }
 
 const char* spec_verify_status_string(sv_status status) {

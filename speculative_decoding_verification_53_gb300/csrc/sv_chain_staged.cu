@@ -1,0 +1,260 @@
+// sv_chain_staged.cu -- chain verify with each CTA's row chunks staged in shared memory.
+//
+// Same rule and the same cluster split as sv_chain.cu ("[논문 리뷰] Fast Inference
+// from Transformers via Speculative Decoding", section 2, Step 3; "Speculative
+// Decoding and EAGLE", section "정확성 규칙"), but the CTA's chunk of the target
+// row (and of the draft-logit row) of position k is brought into shared memory
+// by a bulk copy, so the statistics, the gathered entries at x_k and the
+// replacement draw all read shared memory: every row crosses HBM once.  A ring
+// of `nslot` slots lets a small batch prefetch the next positions while the
+// current one is decided; a large batch uses one slot (no speculative reads) and
+// relies on the other CTAs of the SM to hide latency.  Draft probabilities are
+// only needed at the rejected position: that chunk is copied on demand (after an
+// optional L2 prefetch at kernel start).
+#include "sv_stage.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+
+template <int TDT, int DDT, int DK>
+__global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, const StageLayout L) {
+    extern __shared__ __align__(128) unsigned char dsm[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(dsm);  // [0, nslot): slots; [nslot]: draft-probability area
+    unsigned char* slots = dsm + STAGE_HEADER;
+    unsigned char* probs_area = slots + (size_t)L.nslot * L.slot_bytes;
+    float* tile_sum = reinterpret_cast<float*>(probs_area + L.probs_bytes);
+    __shared__ BlockScratch sc;
+    __shared__ int s_tok[MAX_K];
+    __shared__ float s_r[MAX_K + 1], s_u[MAX_K + 1], s_ap[MAX_K];
+    __shared__ float s_qx;
+
+    const int G = (int)cluster_size(), g = (int)cluster_rank();
+    const int b = blockIdx.y;
+    const int K = a.K, V = a.V;
+    int lo, hi;
+    chunk_range(V, g, G, lo, hi);
+    const int n = hi - lo;
+    const float T = a.temperature ? a.temperature[b] : 0.f;
+    const bool greedy = !(T > 0.f);
+    const float c = greedy ? 0.f : LOG2E / T;
+    constexpr int tsz = TDT == DT_BF16 ? 2 : 4, dsz = DDT == DT_BF16 ? 2 : 4;
+    const bool draft_rows = !greedy && DK == DK_LOGITS;  // draft-logit rows travel with the target rows
+    const unsigned char* tbase = reinterpret_cast<const unsigned char*>(a.target) + (size_t)b * (K + 1) * V * tsz;
+    const unsigned char* dbase = reinterpret_cast<const unsigned char*>(a.draft) + (size_t)b * K * V * dsz;
+
+    int tok_bad = 0;
+    for (int k = threadIdx.x; k < K; k += NT) {
+        const int x = a.tokens[(size_t)b * K + k];
+        s_tok[k] = x;
+        s_ap[k] = -1.f;
+        if (x < 0 || x >= V) tok_bad = 1;
+    }
+    if (!greedy)
+        for (int k = threadIdx.x; k <= K; k += NT)
+            slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, s_r[k], s_u[k]);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i <= L.nslot; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    bool invalid = __syncthreads_or(tok_bad) != 0;
+
+    uint32_t parity = 0, pending = 0;  // per-slot phase parity and copy-in-flight bits (bit nslot: probs area)
+    auto issue = [&](int k) {
+        const int s = k % L.nslot;
+        if (threadIdx.x == 0) {
+            unsigned char* dst = slots + (size_t)s * L.slot_bytes;
+            const uint32_t tb = (uint32_t)n * tsz, db = (draft_rows && k < K) ? (uint32_t)n * dsz : 0u;
+            fence_proxy_async();
+            mbar_arrive_expect_tx(&bars[s], tb + db);
+            if (tb) bulk_g2s(dst, tbase + ((size_t)k * V + lo) * tsz, tb, &bars[s]);
+            if (db) bulk_g2s(dst + L.t_bytes, dbase + ((size_t)k * V + lo) * dsz, db, &bars[s]);
+        }
+        pending |= 1u << s;
+    };
+    auto wait_slot = [&](int s) -> bool {
+        const bool ok = mbar_wait_bounded(&bars[s], (parity >> s) & 1u);
+        parity ^= 1u << s;
+        pending &= ~(1u << s);
+        return ok;
+    };
+
+    int next_issue = 0;
+    if (!invalid) {
+        const int first = (K + 1 < L.nslot) ? K + 1 : L.nslot;
+        for (; next_issue < first; ++next_issue) issue(next_issue);
+        if (DK == DK_PROBS && !greedy && L.prefetch_l2 && threadIdx.x == 0)
+            for (int k = 0; k < K; ++k)
+                if (n) prefetch_l2(dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz);
+    }
+
+    int phase = 0, j = -1, final_tok = -1, writer = 0;
+    for (int k = 0; k <= K && !invalid; ++k) {
+        const int s = k % L.nslot;
+        const int x = k < K ? s_tok[k] : -1;
+        float qx_load = 0.f;  // q(x_k) for draft probabilities, loaded while the copy lands
+        if (DK == DK_PROBS && !greedy && k < K && threadIdx.x == 0)
+            qx_load = __ldg(reinterpret_cast<const float*>(dbase) + (size_t)k * V + x);
+        const int fail = __syncthreads_or(!wait_slot(s));
+        if (DK == DK_PROBS && !greedy && k < K && threadIdx.x == 0) s_qx = qx_load;
+        const unsigned char* tb = slots + (size_t)s * L.slot_bytes;
+        const unsigned char* db = tb + L.t_bytes;
+        if (greedy) {
+            ArgMax am = smem_thread_argmax<TDT>(tb, n, lo);
+            if (fail) am.bad = 1;
+            am = cluster_argmax(am, sc, phase);
+            if (am.bad || !(am.v > neg_inf()) || am.v == pos_inf()) { invalid = true; break; }
+            if (k < K && x == am.i) {
+                if (threadIdx.x == 0) s_ap[k] = 1.f;
+                if (next_issue <= K) issue(next_issue++);
+                continue;
+            }
+            if (k < K && threadIdx.x == 0) s_ap[k] = 0.f;
+            j = k;
+            final_tok = am.i;
+            writer = 0;
+            break;
+        }
+        LSE ts = smem_thread_lse<TDT>(tb, n, c);
+        LSE ds{neg_inf(), 0.f, 0};
+        if (draft_rows && k < K) ds = smem_thread_lse<DDT>(db, n, c);
+        if (fail) ts.bad = 1;
+        float tx = 0.f, dx = 0.f;
+        int has = 0;
+        if (threadIdx.x == 0 && x >= lo && x < hi) {
+            tx = smem_elem<TDT>(tb, x - lo);
+            if (draft_rows) dx = smem_elem<DDT>(db, x - lo);
+            has = 1;
+        }
+        const PosStats ps = cluster_pos_stats(ts, ds, c, tx, dx, has, sc, phase);
+        if (row_bad_s(ps.t) || (draft_rows && k < K && row_bad_s(ps.d))) { invalid = true; break; }
+        const float inv_st = 1.f / ps.t.s;
+        if (k == K) {  // every draft accepted: bonus token from p_K
+            const StagedP<TDT> pw{tb, lo, c, ps.t.m, inv_st};
+            const DrawResult d = cluster_draw(pw, lo, hi, s_u[K], tile_sum, sc, phase);
+            j = K;
+            final_tok = d.token;
+            writer = d.owner;
+            break;
+        }
+        const float px = ex2((ps.tx - ps.t.m) * c) * inv_st;
+        float qx, inv_sd = 0.f;
+        if (DK == DK_LOGITS) {
+            inv_sd = 1.f / ps.d.s;
+            qx = ex2((ps.dx - ps.d.m) * c) * inv_sd;
+        } else {
+            qx = s_qx;
+            if (!(qx >= 0.f) || qx == pos_inf()) { invalid = true; break; }
+        }
+        const float ratio = qx > 0.f ? px / qx : (px > 0.f ? pos_inf() : 0.f);
+        if (threadIdx.x == 0) s_ap[k] = fminf(ratio, 1.f);
+        if (s_r[k] < ratio) {
+            if (next_issue <= K) issue(next_issue++);
+            continue;
+        }
+        // first rejection: replacement from the residual (p_k - q_k)+
+        int dfail = 0;
+        const unsigned char* qb = db;
+        if (DK == DK_PROBS) {
+            if (threadIdx.x == 0 && n) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(&bars[L.nslot], (uint32_t)n * dsz);
+                bulk_g2s(probs_area, dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz, &bars[L.nslot]);
+            } else if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(&bars[L.nslot], 0u);
+            }
+            dfail = __syncthreads_or(!mbar_wait_bounded(&bars[L.nslot], 0u));
+            qb = probs_area;
+        }
+        const StagedResidual<TDT, DDT, DK> rw{tb, qb, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd};
+        DrawResult d = cluster_draw(rw, lo, hi, s_u[k], tile_sum, sc, phase, dfail);
+        if (d.failed) { invalid = true; break; }
+        if (d.owner < 0) {  // the residual has no mass: draw from p_k
+            const StagedP<TDT> pw{tb, lo, c, ps.t.m, inv_st};
+            d = cluster_draw(pw, lo, hi, s_u[k], tile_sum, sc, phase);
+        }
+        j = k;
+        final_tok = d.token;
+        writer = d.owner;
+        break;
+    }
+    // copies still in flight (prefetched positions never reached) must land before the CTA exits
+    for (int s = 0; s < L.nslot; ++s)
+        if (pending & (1u << s)) (void)wait_slot(s);
+    __syncthreads();
+    if (invalid) writer = 0;
+    if (g == writer) {
+        int32_t* ot = a.out_tokens + (size_t)b * (K + 1);
+        for (int i = threadIdx.x; i <= K; i += NT)
+            ot[i] = invalid ? -1 : (i < j ? s_tok[i] : (i == j ? final_tok : -1));
+        if (a.out_accept_prob)
+            for (int i = threadIdx.x; i < K; i += NT)
+                a.out_accept_prob[(size_t)b * K + i] = invalid ? -1.f : s_ap[i];
+        if (threadIdx.x == 0) a.out_count[b] = invalid ? 0 : j + 1;
+    }
+    cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+}
+
+size_t staged_smem_bytes(const StageLayout& L, int V, int G) {
+    return STAGE_HEADER + (size_t)L.nslot * L.slot_bytes + L.probs_bytes + draw_smem_bytes(V, G);
+}
+
+template <int TDT, int DDT, int DK>
+static cudaError_t launch_chain_staged_t(const ChainArgs& a, const StageLayout& L, int G, cudaStream_t stream) {
+    auto kern = chain_staged_kernel<TDT, DDT, DK>;
+    static int max_dyn = -1;  // dynamic shared memory this kernel may request (opt-in limit minus static)
+    if (max_dyn < 0) {
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        const int m = optin - (int)fa.sharedSizeBytes;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, m);
+        if (e != cudaSuccess) return e;
+        max_dyn = m;
+    }
+    const size_t smem = staged_smem_bytes(L, a.V, G);
+    if (smem > (size_t)max_dyn) return cudaErrorInvalidClusterSize;  // caller takes the streaming kernel
+    static size_t cached_smem = 0;
+    static int cached_max = 0;  // largest cluster the device co-schedules at that shared-memory size
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.stream = stream;
+    cfg.dynamicSmemBytes = smem;
+    if (cached_smem != smem) {
+        cfg.gridDim = dim3(MAX_CLUSTER, 1, 1);
+        int m = 0;
+        cudaError_t e = cudaOccupancyMaxPotentialClusterSize(&m, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        cached_max = m;
+        cached_smem = smem;
+    }
+    if (cached_max < G) return cudaErrorInvalidClusterSize;  // caller picks another shape
+    cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, L);
+}
+
+cudaError_t launch_chain_staged(const ChainArgs& a, const StageLayout& L, int tdt, int ddt, int dk, int G,
+                                cudaStream_t stream) {
+    if (dk == DK_PROBS) {
+        if (tdt == DT_BF16) return launch_chain_staged_t<DT_BF16, DT_F32, DK_PROBS>(a, L, G, stream);
+        return launch_chain_staged_t<DT_F32, DT_F32, DK_PROBS>(a, L, G, stream);
+    }
+    if (tdt == DT_BF16) {
+        if (ddt == DT_BF16) return launch_chain_staged_t<DT_BF16, DT_BF16, DK_LOGITS>(a, L, G, stream);
+        return launch_chain_staged_t<DT_BF16, DT_F32, DK_LOGITS>(a, L, G, stream);
+    }
+    if (ddt == DT_BF16) return launch_chain_staged_t<DT_F32, DT_BF16, DK_LOGITS>(a, L, G, stream);
+    return launch_chain_staged_t<DT_F32, DT_F32, DK_LOGITS>(a, L, G, stream);
+}
+
+}  // namespace sv

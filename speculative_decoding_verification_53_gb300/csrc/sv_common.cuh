@@ -291,7 +291,7 @@ __device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
 
 // Per-CTA exchange record published to the cluster (double-buffered by phase).
 struct Xchg {
-    float f[4];
+    float f[8];
     int i[4];
 };
 
@@ -469,11 +469,12 @@ struct DrawResult {
     int owner;
     int token;
     float Z;
+    int failed;  // some CTA reported fail_in (a staging wait that gave up): the draw is void
 };
 
 template <class WF>
 __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float* tile_sum, BlockScratch& sc,
-                                   int& phase) {
+                                   int& phase, int fail_in = 0) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ntiles = (hi - lo + TILE - 1) / TILE;
     for (int t = warp; t < ntiles; t += NW) {
@@ -493,13 +494,21 @@ __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float*
         for (int t = lane; t < ntiles; t += 32) z += tile_sum[t];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        if (lane == 0) slot.f[0] = z;
+        if (lane == 0) {
+            slot.f[0] = z;
+            slot.i[0] = fail_in;
+        }
     }
     cluster_sync_all();
     if (warp == 0) {
         const uint32_t G = cluster_size();
         float z = 0.f;
-        if ((uint32_t)lane < G) z = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
+        int fl = 0;
+        if ((uint32_t)lane < G) {
+            z = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
+            fl = dsmem_ld_s32(dsmem_addr(&slot.i[0], lane));
+        }
+        const int any_fail = __any_sync(0xffffffffu, fl != 0) ? 1 : 0;
         float incl = z;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -513,14 +522,15 @@ __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float*
         int owner = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : -1);
         const float excl = __shfl_sync(0xffffffffu, incl - z, owner < 0 ? 0 : owner);
         if (lane == 0) {
-            sc.bi[0] = (Z > 0.f) ? owner : -1;
+            sc.bi[0] = (Z > 0.f && !any_fail) ? owner : -1;
             sc.bi[1] = hit ? 0 : 1;  // 1: take the last non-zero element of the owner
+            sc.bi[3] = any_fail;
             sc.bf[0] = t - excl;
             sc.bf[1] = Z;
         }
     }
     __syncthreads();
-    DrawResult res{sc.bi[0], -1, sc.bf[1]};
+    DrawResult res{sc.bi[0], -1, sc.bf[1], sc.bi[3]};
     const bool take_last = sc.bi[1] != 0;
     const float t_loc = sc.bf[0];
     __syncthreads();

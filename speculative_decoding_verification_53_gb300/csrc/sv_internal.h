@@ -33,6 +33,22 @@ struct TreeArgs {
     int32_t* out_path;         // [B][D]
 };
 
+// Shared-memory layout of the staged chain kernel (host-computed per launch).
+struct StageLayout {
+    int nslot;        // ring slots, one position's row chunks each (1..16)
+    int slot_bytes;   // bytes per slot: target chunk + draft-logit chunk, 16-byte multiples
+    int t_bytes;      // offset of the draft chunk inside a slot
+    int probs_bytes;  // separate area for the rejected position's draft-probability chunk
+    int prefetch_l2;  // prefetch the draft-probability chunks into L2 at kernel start
+};
+
+constexpr int STAGE_HEADER = 256;        // mbarriers at the start of dynamic shared memory
+constexpr int MAX_DYN_SMEM = 227 * 1024; // opt-in dynamic shared memory per CTA on sm_103a
+
+size_t staged_smem_bytes(const StageLayout& L, int V, int G);
+cudaError_t launch_chain_staged(const ChainArgs& a, const StageLayout& L, int tdt, int ddt, int dk, int cluster,
+                                cudaStream_t stream);
+
 // Cluster size (CTAs per batch row) for a launch over B batch rows.
 int choose_cluster(int B, int V, int num_sms);
 
