@@ -109,6 +109,26 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+_workspaces = {}
+
+
+def _auto_workspace(B, K, V, stream):
+    """A zero-initialised workspace cached per (device, stream) and grown on demand; the
+    library leaves it zeroed after every call, so it is reused as is.  Calls on one stream
+    never overlap, which is what the library requires of a shared workspace."""
+    torch = _torch()
+    need = spec_verify_workspace_size(B, K, V)
+    if need == 0:
+        return None
+    s = torch.cuda.current_stream() if stream is None else stream
+    key = (s.device.index, s.cuda_stream)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=s.device)
+        _workspaces[key] = ws
+    return ws
+
+
 def _kind(draft_kind) -> int:
     if draft_kind in ("probs", SV_DRAFT_PROBS):
         return SV_DRAFT_PROBS
@@ -121,9 +141,11 @@ def _kind(draft_kind) -> int:
 
 def spec_verify_chain(target_logits, draft, draft_tokens, temperature, seed: int, offset: int, *,
                       draft_kind, out_tokens=None, out_count=None, out_accept_prob=None,
-                      want_accept_prob: bool = False, workspace=None, stream=None):
+                      want_accept_prob: bool = False, workspace="auto", stream=None):
     """Chain verify.  target_logits [B][K+1][V] (fp32/bf16), draft [B][K][V] (probs fp32 or
     logits), draft_tokens int32 [B][K], temperature fp32 [B] (T <= 0: greedy row).
+    workspace: "auto" (a cached zeroed buffer per stream), None (none: the kernels that need
+    no scratch), or a caller-owned zero-initialised uint8 CUDA tensor.
     Returns (out_tokens int32 [B][K+1], out_count int32 [B], out_accept_prob fp32 [B][K] or None)."""
     torch = _torch()
     _dev(target_logits, "target_logits")
@@ -143,6 +165,8 @@ def spec_verify_chain(target_logits, draft, draft_tokens, temperature, seed: int
         out_count = torch.empty((B,), dtype=torch.int32, device=dev)
     if out_accept_prob is None and want_accept_prob:
         out_accept_prob = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if isinstance(workspace, str):
+        workspace = _auto_workspace(B, K, V, stream) if B > 0 else None
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
     st = lib().spec_verify_chain(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), ddt, dk,
                                  _ptr(draft_tokens), _ptr(temperature), B, K, V, int(seed), int(offset),

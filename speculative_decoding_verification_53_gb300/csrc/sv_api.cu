@@ -1,6 +1,7 @@
 // sv_api.cu -- the C ABI declared in include/spec_verify.h: argument checks on the
 // host, launch-shape choice, dispatch to the kernels.  Nothing here allocates.
 #include <cstdlib>
+#include <string>
 
 #include "spec_verify.h"
 #include "sv_internal.h"
@@ -52,14 +53,24 @@ sv_status device_info(DeviceInfo& info) {
     return SV_OK;
 }
 
-// SPEC_VERIFY_NO_STAGING=1 forces the register-streaming kernels (for comparison runs).
-bool staging_disabled() {
+// Kernel-family override for comparison runs and tests: SPEC_VERIFY_PATH =
+// "spec" (position-parallel), "staged" (shared-memory staging), "stream"
+// (register streaming); anything else picks automatically.
+enum PathChoice { PATH_AUTO = 0, PATH_SPEC = 1, PATH_STAGED = 2, PATH_STREAM = 3 };
+
+int path_override() {
     static int v = -1;
     if (v < 0) {
-        const char* s = std::getenv("SPEC_VERIFY_NO_STAGING");
-        v = (s && s[0] == '1') ? 1 : 0;
+        const char* s = std::getenv("SPEC_VERIFY_PATH");
+        v = PATH_AUTO;
+        if (s) {
+            const std::string p(s);
+            if (p == "spec") v = PATH_SPEC;
+            if (p == "staged") v = PATH_STAGED;
+            if (p == "stream") v = PATH_STREAM;
+        }
     }
-    return v == 1;
+    return v;
 }
 
 size_t dtype_size(int d) { return d == SV_BF16 ? 2 : 4; }
@@ -96,12 +107,37 @@ sv::StageLayout chain_stage_layout(const void* target, int tdt, const void* draf
     return L;
 }
 
-// Staged kernel when it applies, else the register-streaming kernel.
-sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_draft, int num_sms,
-                    cudaStream_t stream) {
+// Cluster size of the position-parallel kernel: the largest power of two (at most 16)
+// that keeps B * (K + 1) clusters within one CTA per SM.
+int spec_cluster(int B, int K, int num_sms) {
+    int G = 16;
+    while (G > 1 && (long long)B * (K + 1) * G > num_sms) G >>= 1;
+    return G;
+}
+
+// Kernel choice for a chain launch:
+//  - position-parallel (sv_chain_spec.cu) for small batches when a workspace is given:
+//    every position of every row at once, the latency of one position instead of K+1;
+//  - shared-memory staged walk (sv_chain_staged.cu) when rows are 16-byte aligned;
+//  - register-streaming walk (sv_chain.cu) otherwise.
+sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_draft, int num_sms, void* ws,
+                    size_t ws_bytes, cudaStream_t stream) {
+    const int path = path_override();
+    const size_t tsz = dtype_size(tdt), dsz = dk == SV_DRAFT_PROBS ? 4 : dtype_size(ddt);
+    const bool aligned = aligned16(a.target) && (a.V * tsz) % 16 == 0 &&
+                         (!uses_draft || (aligned16(a.draft) && (a.V * dsz) % 16 == 0));
+    if ((path == PATH_AUTO || path == PATH_SPEC) && aligned && ws && ((uintptr_t)ws & 255u) == 0) {
+        const int Gs = spec_cluster(a.B, a.K, num_sms);
+        if ((path == PATH_SPEC || Gs >= 4) && ws_bytes >= sv::spec_workspace_bytes(a.B, a.K, a.V, Gs)) {
+            const cudaError_t e = sv::launch_chain_spec(a, ws, tdt, ddt, dk, Gs, stream);
+            if (e == cudaSuccess) return SV_OK;
+            if (e != cudaErrorInvalidClusterSize) return launch_status(e);
+            (void)cudaGetLastError();
+        }
+    }
     const int G = sv::choose_cluster(a.B, a.V, num_sms);
     const sv::StageLayout L = chain_stage_layout(a.target, tdt, a.draft, ddt, dk, uses_draft, a.B, a.K, a.V, G, num_sms);
-    if (L.nslot > 0 && !staging_disabled()) {
+    if (L.nslot > 0 && path != PATH_STREAM) {
         const cudaError_t e = sv::launch_chain_staged(a, L, tdt, ddt, dk, G, stream);
         if (e == cudaSuccess) return SV_OK;
         if (e != cudaErrorInvalidClusterSize) return launch_status(e);
@@ -118,10 +154,11 @@ namespace sv {
 int choose_cluster(int B, int V, int num_sms) {
     const int forced = cluster_override();
     if (forced) return forced;
-    // Spread each row over enough CTAs that the whole grid holds about two CTAs per
-    // SM, but keep at least 2048 elements per CTA and at most 16 CTAs per row.
+    // As many CTAs per row as keep at least 2048 elements each (at most 16), while the
+    // grid stays within about 16 CTAs per SM: rows are walked position by position, so a
+    // wide split shortens each row's serial chain and many rows in flight hide latency.
     int G = 1;
-    while (G < 16 && (long long)B * G < 2LL * num_sms && V / (2 * G) >= 2048) G *= 2;
+    while (G < 16 && V / (2 * G) >= 2048 && (long long)B * 2 * G <= 16LL * num_sms) G *= 2;
     return G;
 }
 
@@ -130,18 +167,19 @@ int choose_cluster(int B, int V, int num_sms) {
 extern "C" {
 
 size_t spec_verify_workspace_size(int B, int K, int V) {
-    (void)B;
-    (void)K;
-    (void)V;
-    return 0;
+    if (B < 0 || K < 0 || K > kMaxK || V < 1 || V > kMaxV) return 0;
+    size_t need = 0;
+    for (int G = 1; G <= 16; G *= 2) {
+        const size_t b = sv::spec_workspace_bytes(B, K, V, G);
+        if (b > need) need = b;
+    }
+    return need;
 }
 
 sv_status spec_verify_chain(const void* target_logits, sv_dtype tdt, const void* draft, sv_dtype ddt,
                             sv_draft_kind dk, const int32_t* draft_tokens, const float* temperature, int B, int K,
                             int V, uint64_t seed, uint64_t offset, int32_t* out_tokens, int32_t* out_count,
                             float* out_accept_prob, void* workspace, size_t ws_bytes, void* stream) {
-    (void)workspace;
-    (void)ws_bytes;
     if (B < 0 || B > kMaxB || K < 0 || K > kMaxK || V < 1 || V > kMaxV) return SV_ERR_INVALID_ARG;
     if (!is_dtype(tdt) || !is_dtype(ddt)) return SV_ERR_INVALID_ARG;
     if (dk != SV_DRAFT_PROBS && dk != SV_DRAFT_LOGITS) return SV_ERR_INVALID_ARG;
@@ -154,7 +192,7 @@ sv_status spec_verify_chain(const void* target_logits, sv_dtype tdt, const void*
     if (st != SV_OK) return st;
     sv::ChainArgs a{target_logits, draft, draft_tokens, temperature, B, K, V, seed, offset,
                     out_tokens, out_count, out_accept_prob};
-    return run_chain(a, tdt, ddt, dk, K > 0, info.sms, (cudaStream_t)stream);
+    return run_chain(a, tdt, ddt, dk, K > 0, info.sms, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 sv_status spec_greedy_accept(const void* target_logits, sv_dtype tdt, const int32_t* draft_tokens, int B, int K,
@@ -168,7 +206,7 @@ sv_status spec_greedy_accept(const void* target_logits, sv_dtype tdt, const int3
     if (st != SV_OK) return st;
     sv::ChainArgs a{target_logits, nullptr, draft_tokens, nullptr, B, K, V, 0, 0, out_tokens, out_count, nullptr};
     // the draft kind and dtype do not matter for greedy rows; use the smallest instantiation
-    return run_chain(a, tdt, SV_F32, SV_DRAFT_PROBS, false, info.sms, (cudaStream_t)stream);
+    return run_chain(a, tdt, SV_F32, SV_DRAFT_PROBS, false, info.sms, nullptr, 0, (cudaStream_t)stream);
 }
 
 sv_status spec_verify_tree(const void* target_logits, sv_dtype tdt, const void* draft, sv_dtype ddt,

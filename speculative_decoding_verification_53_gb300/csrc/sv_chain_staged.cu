@@ -19,7 +19,11 @@ namespace sv {
 template <int TDT, int DDT, int DK>
 __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, const StageLayout L) {
     extern __shared__ __align__(128) unsigned char dsm[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(dsm);  // [0, nslot): slots; [nslot]: draft-probability area
+    // mbarriers: [0, nslot) target chunks, [nslot, 2 nslot) draft-logit chunks, [2 nslot] probabilities
+    uint64_t* bars = reinterpret_cast<uint64_t*>(dsm);
+    uint64_t* tbar = bars;
+    uint64_t* dbar = bars + L.nslot;
+    uint64_t* pbar = bars + 2 * L.nslot;
     unsigned char* slots = dsm + STAGE_HEADER;
     unsigned char* probs_area = slots + (size_t)L.nslot * L.slot_bytes;
     float* tile_sum = reinterpret_cast<float*>(probs_area + L.probs_bytes);
@@ -34,13 +38,46 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     int lo, hi;
     chunk_range(V, g, G, lo, hi);
     const int n = hi - lo;
+    constexpr int tsz = TDT == DT_BF16 ? 2 : 4, dsz = DDT == DT_BF16 ? 2 : 4;
+    const unsigned char* tbase = reinterpret_cast<const unsigned char*>(a.target) + (size_t)b * (K + 1) * V * tsz;
+    const unsigned char* dbase = reinterpret_cast<const unsigned char*>(a.draft) + (size_t)b * K * V * dsz;
+    const int first = (K + 1 < L.nslot) ? K + 1 : L.nslot;  // positions staged up front
+
+    // The target chunks of the first positions are requested before anything else, so
+    // their HBM latency overlaps the temperature, token and Philox work below.
+    auto issue_t = [&](int k) {
+        const int s = k % L.nslot;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&tbar[s], (uint32_t)n * tsz);
+        if (n) bulk_g2s(slots + (size_t)s * L.slot_bytes, tbase + ((size_t)k * V + lo) * tsz, (uint32_t)n * tsz, &tbar[s]);
+    };
+    auto issue_d = [&](int k) {
+        const int s = k % L.nslot;
+        mbar_arrive_expect_tx(&dbar[s], (uint32_t)n * dsz);
+        if (n)
+            bulk_g2s(slots + (size_t)s * L.slot_bytes + L.t_bytes, dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz,
+                     &dbar[s]);
+    };
+    if (threadIdx.x == 0) {
+        for (int i = 0; i <= 2 * L.nslot; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        for (int k = 0; k < first; ++k) issue_t(k);
+    }
     const float T = a.temperature ? a.temperature[b] : 0.f;
     const bool greedy = !(T > 0.f);
     const float c = greedy ? 0.f : LOG2E / T;
-    constexpr int tsz = TDT == DT_BF16 ? 2 : 4, dsz = DDT == DT_BF16 ? 2 : 4;
     const bool draft_rows = !greedy && DK == DK_LOGITS;  // draft-logit rows travel with the target rows
-    const unsigned char* tbase = reinterpret_cast<const unsigned char*>(a.target) + (size_t)b * (K + 1) * V * tsz;
-    const unsigned char* dbase = reinterpret_cast<const unsigned char*>(a.draft) + (size_t)b * K * V * dsz;
+    if (threadIdx.x == 0) {
+        if (draft_rows)
+            for (int k = 0; k < first && k < K; ++k) issue_d(k);
+        if (DK == DK_PROBS && !greedy && L.prefetch_l2 && n)
+            for (int k = 0; k < K; ++k) prefetch_l2(dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz);
+    }
+    uint32_t tpar = 0, dpar = 0, tpend = 0, dpend = 0;  // per-slot phase parity / copy-in-flight bits
+    for (int k = 0; k < first; ++k) {
+        tpend |= 1u << k;
+        if (draft_rows && k < K) dpend |= 1u << k;
+    }
 
     int tok_bad = 0;
     for (int k = threadIdx.x; k < K; k += NT) {
@@ -52,40 +89,32 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     if (!greedy)
         for (int k = threadIdx.x; k <= K; k += NT)
             slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, s_r[k], s_u[k]);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i <= L.nslot; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
-    }
     bool invalid = __syncthreads_or(tok_bad) != 0;
 
-    uint32_t parity = 0, pending = 0;  // per-slot phase parity and copy-in-flight bits (bit nslot: probs area)
-    auto issue = [&](int k) {
+    auto issue = [&](int k) {  // refill: position k into slot k % nslot (its previous reads are done)
         const int s = k % L.nslot;
         if (threadIdx.x == 0) {
-            unsigned char* dst = slots + (size_t)s * L.slot_bytes;
-            const uint32_t tb = (uint32_t)n * tsz, db = (draft_rows && k < K) ? (uint32_t)n * dsz : 0u;
-            fence_proxy_async();
-            mbar_arrive_expect_tx(&bars[s], tb + db);
-            if (tb) bulk_g2s(dst, tbase + ((size_t)k * V + lo) * tsz, tb, &bars[s]);
-            if (db) bulk_g2s(dst + L.t_bytes, dbase + ((size_t)k * V + lo) * dsz, db, &bars[s]);
+            issue_t(k);
+            if (draft_rows && k < K) issue_d(k);
         }
-        pending |= 1u << s;
+        tpend |= 1u << s;
+        if (draft_rows && k < K) dpend |= 1u << s;
     };
-    auto wait_slot = [&](int s) -> bool {
-        const bool ok = mbar_wait_bounded(&bars[s], (parity >> s) & 1u);
-        parity ^= 1u << s;
-        pending &= ~(1u << s);
+    auto wait_slot = [&](int s) -> bool {  // both chunks of slot s (the draft one only if requested)
+        bool ok = true;
+        if (tpend & (1u << s)) {
+            ok = mbar_wait_bounded(&tbar[s], (tpar >> s) & 1u);
+            tpar ^= 1u << s;
+            tpend &= ~(1u << s);
+        }
+        if (dpend & (1u << s)) {
+            ok = mbar_wait_bounded(&dbar[s], (dpar >> s) & 1u) && ok;
+            dpar ^= 1u << s;
+            dpend &= ~(1u << s);
+        }
         return ok;
     };
-
-    int next_issue = 0;
-    if (!invalid) {
-        const int first = (K + 1 < L.nslot) ? K + 1 : L.nslot;
-        for (; next_issue < first; ++next_issue) issue(next_issue);
-        if (DK == DK_PROBS && !greedy && L.prefetch_l2 && threadIdx.x == 0)
-            for (int k = 0; k < K; ++k)
-                if (n) prefetch_l2(dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz);
-    }
+    int next_issue = first;
 
     int phase = 0, j = -1, final_tok = -1, writer = 0;
     for (int k = 0; k <= K && !invalid; ++k) {
@@ -157,12 +186,12 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
         if (DK == DK_PROBS) {
             if (threadIdx.x == 0 && n) {
                 fence_proxy_async();
-                mbar_arrive_expect_tx(&bars[L.nslot], (uint32_t)n * dsz);
-                bulk_g2s(probs_area, dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz, &bars[L.nslot]);
+                mbar_arrive_expect_tx(pbar, (uint32_t)n * dsz);
+                bulk_g2s(probs_area, dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz, pbar);
             } else if (threadIdx.x == 0) {
-                mbar_arrive_expect_tx(&bars[L.nslot], 0u);
+                mbar_arrive_expect_tx(pbar, 0u);
             }
-            dfail = __syncthreads_or(!mbar_wait_bounded(&bars[L.nslot], 0u));
+            dfail = __syncthreads_or(!mbar_wait_bounded(pbar, 0u));
             qb = probs_area;
         }
         const StagedResidual<TDT, DDT, DK> rw{tb, qb, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd};
@@ -179,7 +208,7 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     }
     // copies still in flight (prefetched positions never reached) must land before the CTA exits
     for (int s = 0; s < L.nslot; ++s)
-        if (pending & (1u << s)) (void)wait_slot(s);
+        if ((tpend | dpend) & (1u << s)) (void)wait_slot(s);
     __syncthreads();
     if (invalid) writer = 0;
     if (g == writer) {

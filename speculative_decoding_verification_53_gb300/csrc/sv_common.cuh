@@ -154,9 +154,19 @@ __device__ __forceinline__ LSE lse_shfl_xor(const LSE& v, int mask) {
     return o;
 }
 
+// Warp all-reduce of (max, sum) pairs: the warp maximum first (no exponentials), then
+// one rescale 2^((m - M) c) per lane and a plain sum, so the dependent chain holds a
+// single exp2 instead of one per shuffle step.  Every lane ends with the warp's pair.
 __device__ __forceinline__ void lse_warp_reduce(LSE& v, float c) {
+    float M = v.m;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lse_merge(v, lse_shfl_xor(v, o), c);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float s = (v.m > neg_inf()) ? v.s * ex2((v.m - M) * c) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    v.bad = __any_sync(0xffffffffu, v.bad != 0) ? 1 : 0;
+    v.m = M;
+    v.s = s;
 }
 
 // One thread's pass over its vector steps of elements [lo, hi) of a row.
@@ -283,6 +293,14 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
     return v;
 }
 
+// Fire-and-forget store into a peer CTA's shared memory (ordered by the next
+// barrier.cluster release/acquire pair).
+__device__ __forceinline__ void dsmem_st_v4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
     int v;
     asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -296,8 +314,25 @@ struct Xchg {
 };
 
 // Shared state of a CTA used by the block- and cluster-level reductions.
+// One warp's (max, sum) partials of the target and draft rows, published to the cluster.
+struct WarpPart {
+    float tm, ts, dm, ds;
+    int bad;  // bit 0: target row NaN, bit 1: draft row NaN
+};
+
+// Inbox of pushed partials: every warp of every CTA of the cluster stores its
+// (target max, target sum, draft max, draft sum) here with a remote store, so after
+// one cluster barrier the combine reads local shared memory only.  A NaN sum marks a
+// row that contained NaN.  Double-buffered by exchange phase.
+struct Inbox {
+    float4 part[2][MAX_CLUSTER][NW];
+    float4 gath[2][MAX_CLUSTER];  // (target value, draft value, has, -) at the drafted token
+};
+
 struct BlockScratch {
     Xchg xchg[2];
+    Inbox inbox;
+    WarpPart wp[2][NW];
     float rf[NW][4];
     int ri[NW][2];
     float bf[8];  // broadcast floats
@@ -366,33 +401,21 @@ __device__ __forceinline__ void cluster_lse2(LSE& a, LSE& b, float c, BlockScrat
 }
 
 __device__ __forceinline__ ArgMax cluster_argmax(ArgMax a, BlockScratch& sc, int& phase) {
+    // Push model (as the statistics combine): lanes 0..G-1 of every warp store the warp's
+    // (max, index, NaN flag) into CTA `lane`'s inbox, then each CTA reduces locally.
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int G = (int)cluster_size(), me = (int)cluster_rank();
+    const int buf = phase & 1;
     argmax_warp_reduce(a);
-    if (lane == 0) {
-        sc.rf[warp][0] = a.v;
-        sc.ri[warp][0] = a.i;
-        sc.ri[warp][1] = a.bad;
-    }
-    __syncthreads();
-    Xchg& slot = sc.xchg[phase & 1];
-    if (warp == 0) {
-        ArgMax x{neg_inf(), 0x7fffffff, 0};
-        if (lane < NW) x = ArgMax{sc.rf[lane][0], sc.ri[lane][0], sc.ri[lane][1]};
-        argmax_warp_reduce(x);
-        if (lane == 0) {
-            slot.f[0] = x.v;
-            slot.i[0] = x.i;
-            slot.i[1] = x.bad;
-        }
-    }
+    if (lane < G)
+        dsmem_st_v4(dsmem_addr(&sc.inbox.part[buf][me][warp], (uint32_t)lane),
+                    make_float4(a.v, __int_as_float(a.i), __int_as_float(a.bad), 0.f));
     cluster_sync_all();
     if (warp == 0) {
-        const uint32_t G = cluster_size();
         ArgMax x{neg_inf(), 0x7fffffff, 0};
-        if ((uint32_t)lane < G) {
-            x.v = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
-            x.i = dsmem_ld_s32(dsmem_addr(&slot.i[0], lane));
-            x.bad = dsmem_ld_s32(dsmem_addr(&slot.i[1], lane));
+        for (int e = lane; e < G * NW; e += 32) {
+            const float4 v = sc.inbox.part[buf][e / NW][e % NW];
+            argmax_merge(x, ArgMax{v.x, __float_as_int(v.y), __float_as_int(v.z)});
         }
         argmax_warp_reduce(x);
         if (lane == 0) {

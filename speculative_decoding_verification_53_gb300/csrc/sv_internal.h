@@ -42,12 +42,17 @@ struct StageLayout {
     int prefetch_l2;  // prefetch the draft-probability chunks into L2 at kernel start
 };
 
-constexpr int STAGE_HEADER = 256;        // mbarriers at the start of dynamic shared memory
+constexpr int STAGE_HEADER = 512;        // mbarriers (up to 2 * 16 + 1) at the start of dynamic shared memory
 constexpr int MAX_DYN_SMEM = 227 * 1024; // opt-in dynamic shared memory per CTA on sm_103a
 
 size_t staged_smem_bytes(const StageLayout& L, int V, int G);
 cudaError_t launch_chain_staged(const ChainArgs& a, const StageLayout& L, int tdt, int ddt, int dk, int cluster,
                                 cudaStream_t stream);
+
+// Position-parallel chain kernel (small batches): workspace bytes and launch.
+size_t spec_workspace_bytes(int B, int K, int V, int G);
+size_t spec_smem_bytes(int V, int K, int G, int tsz, int dsz, int* t_bytes, int* d_bytes, int* fin_off);
+cudaError_t launch_chain_spec(const ChainArgs& a, void* ws, int tdt, int ddt, int dk, int cluster, cudaStream_t stream);
 
 // Cluster size (CTAs per batch row) for a launch over B batch rows.
 int choose_cluster(int B, int V, int num_sms);

@@ -98,29 +98,29 @@ __device__ __forceinline__ float smem_elem(const unsigned char* buf, int e) {
                            : reinterpret_cast<const float*>(buf)[e];
 }
 
-// Online (max, sum 2^((l - max) c)) of the n staged elements, one thread's share.
+// (max, sum 2^((l - max) c)) of one thread's share of the n staged elements, in two
+// passes over shared memory: the maximum first, then independent exponentials with
+// no rescaling, so the exp2 instructions of different vectors overlap.
 template <int DT>
 __device__ __forceinline__ LSE smem_thread_lse(const unsigned char* buf, int n, float c) {
-    LSE acc{neg_inf(), 0.f, 0};
+    float m = neg_inf();
     for (int e = (int)threadIdx.x * VEC; e < n; e += NT * VEC) {
         float x[VEC];
         smem_load8<DT>(buf, e, n, neg_inf(), x);
-        const float vm = vmax8(x);
-        if (vm != vm) acc.bad = 1;
-        if (vm > acc.m) {
-            acc.s *= ex2((acc.m - vm) * c);
-            acc.m = vm;
-        }
-        if (acc.m > neg_inf()) {
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int j = 0; j < VEC; j += 2) {
-                s0 += ex2((x[j] - acc.m) * c);
-                s1 += ex2((x[j + 1] - acc.m) * c);
-            }
-            acc.s += s0 + s1;
-        }
+        m = fmax_nan(m, vmax8(x));
     }
+    LSE acc{m, 0.f, m != m ? 1 : 0};
+    if (!(m > neg_inf()) || acc.bad) return acc;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    for (int e = (int)threadIdx.x * VEC; e < n; e += NT * VEC) {
+        float x[VEC];
+        smem_load8<DT>(buf, e, n, neg_inf(), x);
+        s0 += ex2((x[0] - m) * c) + ex2((x[4] - m) * c);
+        s1 += ex2((x[1] - m) * c) + ex2((x[5] - m) * c);
+        s2 += ex2((x[2] - m) * c) + ex2((x[6] - m) * c);
+        s3 += ex2((x[3] - m) * c) + ex2((x[7] - m) * c);
+    }
+    acc.s = (s0 + s1) + (s2 + s3);
     return acc;
 }
 
@@ -159,53 +159,43 @@ struct PosStats {
 
 __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, float tx, float dx, int has,
                                                       BlockScratch& sc, int& phase) {
+    // Push model: lanes 0..G-1 of every warp store the warp's partials into CTA
+    // `lane`'s inbox; thread 0 also pushes the values it gathered at x_k.  One
+    // cluster barrier later each CTA combines its own inbox from local memory.
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int G = (int)cluster_size(), me = (int)cluster_rank();
+    const int buf = phase & 1;
     lse_warp_reduce(t, c);
     lse_warp_reduce(d, c);
-    if (lane == 0) {
-        sc.rf[warp][0] = t.m; sc.rf[warp][1] = t.s;
-        sc.rf[warp][2] = d.m; sc.rf[warp][3] = d.s;
-        sc.ri[warp][0] = t.bad; sc.ri[warp][1] = d.bad;
+    if (lane < G) {
+        const float4 v = make_float4(t.m, t.bad ? __int_as_float(0x7fffffff) : t.s, d.m,
+                                     d.bad ? __int_as_float(0x7fffffff) : d.s);
+        dsmem_st_v4(dsmem_addr(&sc.inbox.part[buf][me][warp], (uint32_t)lane), v);
     }
-    __syncthreads();
-    Xchg& slot = sc.xchg[phase & 1];
     if (warp == 0) {
-        LSE x{neg_inf(), 0.f, 0}, y{neg_inf(), 0.f, 0};
-        if (lane < NW) {
-            x = LSE{sc.rf[lane][0], sc.rf[lane][1], sc.ri[lane][0]};
-            y = LSE{sc.rf[lane][2], sc.rf[lane][3], sc.ri[lane][1]};
-        }
-        lse_warp_reduce(x, c);
-        lse_warp_reduce(y, c);
-        if (lane == 0) {
-            slot.f[0] = x.m; slot.f[1] = x.s; slot.f[2] = y.m; slot.f[3] = y.s;
-            slot.f[4] = tx; slot.f[5] = dx;
-            slot.i[0] = x.bad; slot.i[1] = y.bad; slot.i[2] = has;
-        }
+        const float gtx = __shfl_sync(0xffffffffu, tx, 0), gdx = __shfl_sync(0xffffffffu, dx, 0);
+        const int ghas = __shfl_sync(0xffffffffu, has, 0);
+        if (lane < G)
+            dsmem_st_v4(dsmem_addr(&sc.inbox.gath[buf][me], (uint32_t)lane), make_float4(gtx, gdx, (float)ghas, 0.f));
     }
     cluster_sync_all();
     if (warp == 0) {
-        const uint32_t G = cluster_size();
         LSE x{neg_inf(), 0.f, 0}, y{neg_inf(), 0.f, 0};
-        float gx = 0.f, gd = 0.f;
-        int h = 0;
-        if ((uint32_t)lane < G) {
-            x.m = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
-            x.s = dsmem_ld_f32(dsmem_addr(&slot.f[1], lane));
-            y.m = dsmem_ld_f32(dsmem_addr(&slot.f[2], lane));
-            y.s = dsmem_ld_f32(dsmem_addr(&slot.f[3], lane));
-            gx = dsmem_ld_f32(dsmem_addr(&slot.f[4], lane));
-            gd = dsmem_ld_f32(dsmem_addr(&slot.f[5], lane));
-            x.bad = dsmem_ld_s32(dsmem_addr(&slot.i[0], lane));
-            y.bad = dsmem_ld_s32(dsmem_addr(&slot.i[1], lane));
-            h = dsmem_ld_s32(dsmem_addr(&slot.i[2], lane));
+        for (int e = lane; e < G * NW; e += 32) {
+            const float4 v = sc.inbox.part[buf][e / NW][e % NW];
+            LSE px{v.x, v.y, v.y != v.y ? 1 : 0}, py{v.z, v.w, v.w != v.w ? 1 : 0};
+            if (px.bad) px.s = 0.f;
+            if (py.bad) py.s = 0.f;
+            lse_merge(x, px, c);
+            lse_merge(y, py, c);
         }
         lse_warp_reduce(x, c);
         lse_warp_reduce(y, c);
-        const unsigned owners = __ballot_sync(0xffffffffu, h != 0);
+        float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane < G) gv = sc.inbox.gath[buf][lane];
+        const unsigned owners = __ballot_sync(0xffffffffu, gv.z != 0.f);
         const int src = owners ? __ffs(owners) - 1 : 0;
-        gx = __shfl_sync(0xffffffffu, gx, src);
-        gd = __shfl_sync(0xffffffffu, gd, src);
+        const float gx = __shfl_sync(0xffffffffu, gv.x, src), gd = __shfl_sync(0xffffffffu, gv.y, src);
         if (lane == 0) {
             sc.bf[0] = x.m; sc.bf[1] = x.s; sc.bf[2] = y.m; sc.bf[3] = y.s;
             sc.bf[4] = gx; sc.bf[5] = gd;
@@ -219,7 +209,6 @@ __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, flo
     r.tx = sc.bf[4];
     r.dx = sc.bf[5];
     r.found = sc.bi[2];
-    __syncthreads();
     ++phase;
     return r;
 }

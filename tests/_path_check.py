@@ -1,0 +1,34 @@
+"""Run a set of chain parity checks in this process (used by test_gpu_paths.py with
+SPEC_VERIFY_PATH set in the environment, which the library reads once)."""
+import os
+import sys
+
+import numpy as np
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+from speculative_decoding_verification_53_gb300 import synth  # noqa: E402
+from _harness import compare, gpu_chain, oracle_chain  # noqa: E402
+
+
+def main():
+    excused = 0
+    w = synth.mixed_batch(seed=11, B=6, K=5, V=32000)
+    excused += compare(gpu_chain(w, seed=3), oracle_chain(w, seed=3))
+    w0 = synth.single_stream(seed=2, B=6)
+    for s in range(6):
+        ws = {k: (v[s:s + 1] if isinstance(v, np.ndarray) else v) for k, v in w0.items()}
+        excused += compare(gpu_chain(ws, seed=s, offset=s), oracle_chain(ws, seed=s, offset=s))
+    w = synth.large_batch(seed=4, temperature=1.0, sigma=1.0, B=3, K=8)
+    excused += compare(gpu_chain(w, seed=9), oracle_chain(w, seed=9))
+    w = synth.tiny_chain(seed=8, V=4096, K=0, B=2)
+    excused += compare(gpu_chain(w), oracle_chain(w))
+    w = synth.tiny_chain(seed=9, V=1024, K=64, B=1, sigma=0.1)
+    excused += compare(gpu_chain(w), oracle_chain(w))
+    assert excused <= 2, excused
+    print("ok", excused)
+
+
+if __name__ == "__main__":
+    main()
