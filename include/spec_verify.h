@@ -118,6 +118,30 @@ SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt,
                             void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Chain verify that allocates nothing (the pages have no counterpart: this is a
+ * deployment convenience).  For callers that cannot hand the library a workspace:
+ * code running inside a runtime that owns every device allocation (an engine's
+ * memory arena, a plugin interface that passes only input and output buffers) or a
+ * path on which no allocation call is allowed.  Same arguments, outputs and results
+ * as spec_verify_chain, minus the workspace: the scratch is a 2 MiB array inside
+ * the library's device image, present on every device that loads the library until
+ * the process exits.  No cudaMalloc, cudaFree or other allocating call is made.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current) and zeroes it synchronously;
+ *     make that first call before any stream capture.
+ *   - Calls whose scratch would exceed 2 MiB (spec_verify_workspace_size(B, K, V) >
+ *     2 MiB) return SV_ERR_UNSUPPORTED without launching anything.
+ *   - Every call shares the one array: calls that overlap on the GPU (different
+ *     streams, or different host threads) race and must be serialised by the caller.
+ */
+SV_API sv_status spec_verify_chain_noalloc(const void *target_logits, sv_dtype tdt,
+                                    const void *draft, sv_dtype ddt, sv_draft_kind dk,
+                                    const int32_t *draft_tokens, const float *temperature,
+                                    int B, int K, int V, uint64_t seed, uint64_t offset,
+                                    int32_t *out_tokens, int32_t *out_count, float *out_accept_prob,
+                                    void *stream);
+
+/*
  * Greedy acceptance (the temperature-0 rule) for every row:
  *   target_logits device [B][K+1][V] (tdt), draft_tokens device int32 [B][K];
  *   out_tokens device int32 [B][K+1], out_count device int32 [B].

@@ -23,7 +23,7 @@ SV_F32, SV_BF16 = 0, 1
 SV_DRAFT_PROBS, SV_DRAFT_LOGITS = 0, 1
 
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_chain", "spec_greedy_accept", "spec_verify_tree",
-           "spec_verify_status_string", "spec_verify_last_cuda_error")
+           "spec_verify_status_string", "spec_verify_last_cuda_error", "spec_verify_chain_noalloc")
 
 _lib = None
 
@@ -51,6 +51,8 @@ def lib() -> ctypes.CDLL:
     L.spec_verify_workspace_size.restype = sz
     L.spec_verify_chain.argtypes = [vp, ci, vp, ci, ci, vp, vp, ci, ci, ci, u64, u64, vp, vp, vp, vp, sz, vp]
     L.spec_verify_chain.restype = ci
+    L.spec_verify_chain_noalloc.argtypes = [vp, ci, vp, ci, ci, vp, vp, ci, ci, ci, u64, u64, vp, vp, vp, vp]
+    L.spec_verify_chain_noalloc.restype = ci
     L.spec_greedy_accept.argtypes = [vp, ci, vp, ci, ci, ci, vp, vp, vp]
     L.spec_greedy_accept.restype = ci
     L.spec_verify_tree.argtypes = [vp, ci, vp, ci, ci, vp, vp, vp, ci, ci, ci, ci, u64, u64, vp, vp, vp, vp]
@@ -174,6 +176,36 @@ def spec_verify_chain(target_logits, draft, draft_tokens, temperature, seed: int
                                  _stream(stream))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_chain")
+    return out_tokens, out_count, out_accept_prob
+
+
+def spec_verify_chain_noalloc(target_logits, draft, draft_tokens, temperature, seed: int, offset: int, *,
+                              draft_kind, out_tokens=None, out_count=None, out_accept_prob=None,
+                              want_accept_prob: bool = False, stream=None):
+    """spec_verify_chain for callers that cannot provide a workspace: the library uses a
+    fixed 2 MiB scratch array of its own (first call on a device sets it up, so make it
+    before any graph capture; overlapping calls race).  Same arguments and results."""
+    torch = _torch()
+    _dev(target_logits, "target_logits")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    dk = _kind(draft_kind)
+    _dev(draft, "draft")
+    _dev(draft_tokens, "draft_tokens", torch.int32)
+    _dev(temperature, "temperature", torch.float32)
+    ddt = SV_F32 if draft is None else _dtype_code(draft)
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_count is None:
+        out_count = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_accept_prob is None and want_accept_prob:
+        out_accept_prob = torch.empty((B, K), dtype=torch.float32, device=dev)
+    st = lib().spec_verify_chain_noalloc(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), ddt, dk,
+                                         _ptr(draft_tokens), _ptr(temperature), B, K, V, int(seed), int(offset),
+                                         _ptr(out_tokens), _ptr(out_count), _ptr(out_accept_prob), _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_chain_noalloc")
     return out_tokens, out_count, out_accept_prob
 
 

@@ -151,6 +151,15 @@ sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_
 
 namespace sv {
 
+sv_status chain_with_scratch(const void* target_logits, int tdt, const void* draft, int ddt, int dk,
+                             const int32_t* draft_tokens, const float* temperature, int B, int K, int V,
+                             uint64_t seed, uint64_t offset, int32_t* out_tokens, int32_t* out_count,
+                             float* out_accept_prob, void* scratch, size_t scratch_bytes, void* stream) {
+    return spec_verify_chain(target_logits, (sv_dtype)tdt, draft, (sv_dtype)ddt, (sv_draft_kind)dk, draft_tokens,
+                             temperature, B, K, V, seed, offset, out_tokens, out_count, out_accept_prob, scratch,
+                             scratch_bytes, stream);
+}
+
 int choose_cluster(int B, int V, int num_sms) {
     const int forced = cluster_override();
     if (forced) return forced;

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "spec_verify.h"
+
 namespace sv {
 
 struct ChainArgs {
@@ -53,6 +55,13 @@ cudaError_t launch_chain_staged(const ChainArgs& a, const StageLayout& L, int td
 size_t spec_workspace_bytes(int B, int K, int V, int G);
 size_t spec_smem_bytes(int V, int K, int G, int tsz, int dsz, int* t_bytes, int* d_bytes, int* fin_off);
 cudaError_t launch_chain_spec(const ChainArgs& a, void* ws, int tdt, int ddt, int dk, int cluster, cudaStream_t stream);
+
+// spec_verify_chain with the workspace supplied by the library itself (used by the
+// entry point that allocates nothing).
+sv_status chain_with_scratch(const void* target_logits, int tdt, const void* draft, int ddt, int dk,
+                             const int32_t* draft_tokens, const float* temperature, int B, int K, int V,
+                             uint64_t seed, uint64_t offset, int32_t* out_tokens, int32_t* out_count,
+                             float* out_accept_prob, void* scratch, size_t scratch_bytes, void* stream);
 
 // Cluster size (CTAs per batch row) for a launch over B batch rows.
 int choose_cluster(int B, int V, int num_sms);
