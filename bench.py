@@ -106,17 +106,20 @@ def measured_peak():
 
 
 def profile_traffic(workload: str):
-    """DRAM bytes per launch of the timed kernel from the committed ncu summary, if the
-    kernel sources still hash to the value recorded there (else None)."""
-    path = os.path.join(ROOT, "profiles", f"chain_kernel_{workload}.md")
-    if not os.path.exists(path):
-        return None, None
-    text = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    hm = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    if not m or not hm or hm.group(1) != kernel_source_hash():
-        return None, path
-    return float(m.group(1)), path
+    """DRAM bytes per launch of the timed kernel from the committed ncu summary for this
+    workload (profiles/<kernel>_<workload>.md), if the kernel sources still hash to the
+    value recorded there; else None.  Returns (bytes, summary path, kernel name)."""
+    import glob
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"*_{workload}.md"))):
+        text = open(path).read()
+        m = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        hm = re.search(r"^kernel_source_sha:\s*([0-9a-f]+)", text, re.M)
+        km = re.search(r"^kernel:\s*(\S+)", text, re.M)
+        kernel = km.group(1) if km else None
+        if not m or not hm or hm.group(1) != kernel_source_hash():
+            return None, os.path.relpath(path, ROOT), kernel
+        return float(m.group(1)), os.path.relpath(path, ROOT), kernel
+    return None, None, None
 
 
 class ClockSampler:
@@ -331,7 +334,7 @@ def run_ours(args, rank, world, device):
         return None
     peak, peak_src = measured_peak()
     achieved = bytes_per_launch / (ms_per_step / 1e3) / 1e9
-    traffic, prof = profile_traffic(args.workload)
+    traffic, prof, prof_kernel = profile_traffic(args.workload)
     line = {
         "metric": METRIC,
         "value": value,
@@ -354,7 +357,7 @@ def run_ours(args, rank, world, device):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (STREAM copy)",
                      "algorithmic_bytes_per_launch": bytes_per_launch,
-                     "kernel": "tree_kernel" if tree else "chain_kernel",
+                     "kernel": prof_kernel or ("tree_kernel" if tree else "chain kernel chosen by the library"),
                      "traffic_source": prof},
         "e2e": e2e,
         "cpu_baseline": cpu,
