@@ -47,7 +47,7 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 
 # ------------------------------------------------------------------ inputs
 
-def make_workload(name: str, rank: int, rounds: int, batch: int = 0):
+def make_workload(name: str, rank: int, rounds: int, batch: int = 0, temperature=None):
     from speculative_decoding_verification_53_gb300 import synth
     seed = 1000 + rank
     if name == "single_stream":
@@ -56,8 +56,9 @@ def make_workload(name: str, rank: int, rounds: int, batch: int = 0):
                                              "bf16 target logits, fp32 draft probabilities")
     if name == "large_batch":
         B = batch or 256
-        w = synth.large_batch(seed=seed, temperature=0.7, sigma=1.0, B=B)
-        return dict(w, per_step_rows=B, desc=f"large-batch chain verify B={B} K=8 V=152064 T=0.7, "
+        T = 0.7 if temperature is None else temperature
+        w = synth.large_batch(seed=seed, temperature=T, sigma=1.0, B=B)
+        return dict(w, per_step_rows=B, desc=f"large-batch chain verify B={B} K=8 V=152064 T={T:g}, "
                                              "bf16 target and draft logits, draft noise sigma=1")
     if name == "mixed_batch":
         w = synth.mixed_batch(seed=seed)
@@ -226,7 +227,7 @@ def run_ours(args, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     sv.lib()
-    w = make_workload(args.workload, rank, args.rounds, args.batch)
+    w = make_workload(args.workload, rank, args.rounds, args.batch, args.temperature)
     tree = w["kind"] == "tree"
     per_step_rows = w["per_step_rows"]
     stream = torch.cuda.Stream(device)
@@ -449,7 +450,7 @@ def run_reference(args, rank):
         return None
     import oracle
     oracle.build()
-    w = make_workload(args.workload, 0, args.rounds, args.batch)
+    w = make_workload(args.workload, 0, args.rounds, args.batch, args.temperature)
     per_step_rows = w["per_step_rows"]
     n_inputs = w["target"].shape[0] // per_step_rows
     tree = w["kind"] == "tree"
@@ -476,7 +477,7 @@ def run_reference(args, rank):
         done += 1
     el = time.perf_counter() - t0
     value = done * per_step_rows / el
-    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": done,
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": done,
             "warmup": max(args.warmup, 3), "ms_per_step": el / max(done, 1) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": w["desc"], "batch_rows_per_step": per_step_rows,
@@ -499,6 +500,7 @@ def main():
     ap.add_argument("--rounds", type=int, default=64, help="resident rounds of the single-stream workload")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--batch", type=int, default=0, help="batch rows of the large-batch workload (default 256)")
+    ap.add_argument("--temperature", type=float, default=None, help="temperature of the large-batch workload")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -239,6 +239,28 @@ sv_status spec_verify_tree(const void* target_logits, sv_dtype tdt, const void* 
     sv::TreeArgs a{target_logits, draft, node_tokens, parent, temperature, B, N, V, max_depth, seed, offset,
                    out_tokens, out_count, out_path};
     const int G = sv::choose_cluster(B, V, info.sms);
+    // shared-memory staged walk (with the children's rows prefetched) when rows are aligned
+    const size_t tsz = dtype_size(tdt), dsz = dk == SV_DRAFT_PROBS ? 4 : dtype_size(ddt);
+    if (path_override() != PATH_STREAM && aligned16(target_logits) && aligned16(draft) && (V * tsz) % 16 == 0 &&
+        (V * dsz) % 16 == 0) {
+        const size_t nvec = (V + 7) / 8, cmax = ((nvec + G - 1) / G) * 8;
+        sv::StageLayout L{0, 0, 0, 0, 0};
+        L.t_bytes = (int)round16(cmax * tsz);
+        L.slot_bytes = L.t_bytes + (int)round16(cmax * dsz);
+        const bool small = (long long)B * G <= info.sms;
+        const size_t budget = small ? (size_t)sv::MAX_DYN_SMEM - 48 * 1024 : (size_t)90 * 1024;
+        const size_t fixed = sv::STAGE_HEADER + sv::draw_smem_bytes(V, G);
+        if (fixed + L.slot_bytes <= budget) {
+            size_t nslot = (budget - fixed) / L.slot_bytes;
+            if (nslot > 16) nslot = 16;
+            if (!small && nslot > 2) nslot = 2;
+            L.nslot = (int)nslot;
+            const cudaError_t e = sv::launch_tree_staged(a, L, tdt, ddt, dk, G, (cudaStream_t)stream);
+            if (e == cudaSuccess) return SV_OK;
+            if (e != cudaErrorInvalidClusterSize) return launch_status(e);
+            (void)cudaGetLastError();
+        }
+    }
     return launch_status(sv::launch_tree(a, tdt, ddt, dk, G, (cudaStream_t)stream));
 }
 

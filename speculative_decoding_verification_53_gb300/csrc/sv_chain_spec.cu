@@ -71,10 +71,11 @@ struct SpecArgs {
 template <int DK>
 __device__ __forceinline__ void spec_weights8(const float l[VEC], const float d[VEC], float c, float mt, float inv_st,
                                               float md, float inv_sd, float w_res[VEC], float w_p[VEC]) {
+    const float mtc = __fmul_rn(mt, c), mdc = __fmul_rn(md, c);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
-        const float p = __fmul_rn(ex2(__fmul_rn(__fsub_rn(l[j], mt), c)), inv_st);
-        const float q = (DK == DK_LOGITS) ? __fmul_rn(ex2(__fmul_rn(__fsub_rn(d[j], md), c)), inv_sd) : d[j];
+        const float p = __fmul_rn(ex2(__fmaf_rn(l[j], c, -mtc)), inv_st);
+        const float q = (DK == DK_LOGITS) ? __fmul_rn(ex2(__fmaf_rn(d[j], c, -mdc)), inv_sd) : d[j];
         w_p[j] = p;
         w_res[j] = fmaxf(__fsub_rn(p, q), 0.f);
     }

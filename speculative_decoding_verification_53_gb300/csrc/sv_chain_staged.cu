@@ -86,9 +86,10 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
         s_ap[k] = -1.f;
         if (x < 0 || x >= V) tok_bad = 1;
     }
-    if (!greedy)
-        for (int k = threadIdx.x; k <= K; k += NT)
-            slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, s_r[k], s_u[k]);
+    // Philox blocks on warps 1.. (warp 0 issues the copies), independent of the temperature
+    // so that they overlap the loads; greedy rows simply never use them
+    for (int k = (int)threadIdx.x - 32; k >= 0 && k <= K; k += NT - 32)
+        slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, s_r[k], s_u[k]);
     bool invalid = __syncthreads_or(tok_bad) != 0;
 
     auto issue = [&](int k) {  // refill: position k into slot k % nslot (its previous reads are done)

@@ -51,6 +51,9 @@ size_t staged_smem_bytes(const StageLayout& L, int V, int G);
 cudaError_t launch_chain_staged(const ChainArgs& a, const StageLayout& L, int tdt, int ddt, int dk, int cluster,
                                 cudaStream_t stream);
 
+cudaError_t launch_tree_staged(const TreeArgs& a, const StageLayout& L, int tdt, int ddt, int dk, int cluster,
+                               cudaStream_t stream);
+
 // Position-parallel chain kernel (small batches): workspace bytes and launch.
 size_t spec_workspace_bytes(int B, int K, int V, int G);
 size_t spec_smem_bytes(int V, int K, int G, int tsz, int dsz, int* t_bytes, int* d_bytes, int* fin_off);

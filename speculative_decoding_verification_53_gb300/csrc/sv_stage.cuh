@@ -31,6 +31,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Raise the expected transaction bytes of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
@@ -98,27 +104,57 @@ __device__ __forceinline__ float smem_elem(const unsigned char* buf, int e) {
                            : reinterpret_cast<const float*>(buf)[e];
 }
 
-// (max, sum 2^((l - max) c)) of one thread's share of the n staged elements, in two
-// passes over shared memory: the maximum first, then independent exponentials with
-// no rescaling, so the exp2 instructions of different vectors overlap.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Maximum of one thread's share of the n staged elements (NaN propagates).  bf16 rows
+// are scanned as packed pairs: three max.bf16x2 per 16-byte vector, no unpacking.
 template <int DT>
-__device__ __forceinline__ LSE smem_thread_lse(const unsigned char* buf, int n, float c) {
+__device__ __forceinline__ float smem_thread_max(const unsigned char* buf, int n) {
+    if (DT == DT_BF16) {
+        uint32_t acc = 0xff80ff80u;  // (-inf, -inf)
+        int e = (int)threadIdx.x * VEC;
+        for (; e + VEC <= n; e += NT * VEC) {
+            const uint4 v = *reinterpret_cast<const uint4*>(buf + (size_t)e * 2);
+            acc = bmax2_nan(acc, bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w)));
+        }
+        float m = fmax_nan(bf16_lo(acc), bf16_hi(acc));
+        if (e < n) {  // a partial last vector
+            float x[VEC];
+            smem_load8<DT>(buf, e, n, neg_inf(), x);
+            m = fmax_nan(m, vmax8(x));
+        }
+        return m;
+    }
     float m = neg_inf();
     for (int e = (int)threadIdx.x * VEC; e < n; e += NT * VEC) {
         float x[VEC];
         smem_load8<DT>(buf, e, n, neg_inf(), x);
         m = fmax_nan(m, vmax8(x));
     }
+    return m;
+}
+
+// (max, sum 2^((l - max) c)) of one thread's share of the n staged elements, in two
+// passes over shared memory: the maximum first, then independent exponentials with
+// no rescaling, each argument a single FFMA l*c - max*c.
+template <int DT>
+__device__ __forceinline__ LSE smem_thread_lse(const unsigned char* buf, int n, float c) {
+    const float m = smem_thread_max<DT>(buf, n);
     LSE acc{m, 0.f, m != m ? 1 : 0};
     if (!(m > neg_inf()) || acc.bad) return acc;
+    const float mc = m * c;
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
     for (int e = (int)threadIdx.x * VEC; e < n; e += NT * VEC) {
         float x[VEC];
         smem_load8<DT>(buf, e, n, neg_inf(), x);
-        s0 += ex2((x[0] - m) * c) + ex2((x[4] - m) * c);
-        s1 += ex2((x[1] - m) * c) + ex2((x[5] - m) * c);
-        s2 += ex2((x[2] - m) * c) + ex2((x[6] - m) * c);
-        s3 += ex2((x[3] - m) * c) + ex2((x[7] - m) * c);
+        s0 += ex2(fmaf(x[0], c, -mc)) + ex2(fmaf(x[4], c, -mc));
+        s1 += ex2(fmaf(x[1], c, -mc)) + ex2(fmaf(x[5], c, -mc));
+        s2 += ex2(fmaf(x[2], c, -mc)) + ex2(fmaf(x[6], c, -mc));
+        s3 += ex2(fmaf(x[3], c, -mc)) + ex2(fmaf(x[7], c, -mc));
     }
     acc.s = (s0 + s1) + (s2 + s3);
     return acc;
@@ -222,8 +258,9 @@ struct StagedP {  // w = p = 2^((l - m) c) / S
     __device__ __forceinline__ void eval8(int e0, int hi, float w[VEC]) const {
         float l[VEC];
         smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
+        const float mc = m * c;
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) w[j] = ex2((l[j] - m) * c) * inv_s;
+        for (int j = 0; j < VEC; ++j) w[j] = ex2(fmaf(l[j], c, -mc)) * inv_s;
     }
 };
 
@@ -237,10 +274,11 @@ struct StagedResidual {  // w = max(0, p - q)
         float l[VEC], d[VEC];
         smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
         smem_load8<DDT>(db, e0 - lo, hi - lo, DK == DK_LOGITS ? neg_inf() : 0.f, d);
+        const float mtc = mt * c, mdc = md * c;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-            const float p = ex2((l[j] - mt) * c) * inv_st;
-            const float q = (DK == DK_LOGITS) ? ex2((d[j] - md) * c) * inv_sd : d[j];
+            const float p = ex2(fmaf(l[j], c, -mtc)) * inv_st;
+            const float q = (DK == DK_LOGITS) ? ex2(fmaf(d[j], c, -mdc)) * inv_sd : d[j];
             w[j] = fmaxf(p - q, 0.f);
         }
     }

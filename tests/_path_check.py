@@ -9,7 +9,7 @@ sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 
 from speculative_decoding_verification_53_gb300 import synth  # noqa: E402
-from _harness import compare, gpu_chain, oracle_chain  # noqa: E402
+from _harness import compare, gpu_chain, gpu_tree, oracle_chain, oracle_tree  # noqa: E402
 
 
 def main():
@@ -26,6 +26,12 @@ def main():
     excused += compare(gpu_chain(w), oracle_chain(w))
     w = synth.tiny_chain(seed=9, V=1024, K=64, B=1, sigma=0.1)
     excused += compare(gpu_chain(w), oracle_chain(w))
+    tw = synth.tree(seed=6, B=4, N=24, V=8192, max_depth=5)
+    for T in (0.0, 1.0):
+        tw["temperature"] = np.full(4, T, np.float32)
+        excused += compare(gpu_tree(tw, seed=2), oracle_tree(tw, seed=2), keys=("tokens", "count", "path"))
+    cw = synth.chain_as_tree(synth.tiny_chain(seed=7, V=2048, K=6, B=8, temperature=0.8))
+    excused += compare(gpu_tree(cw, seed=4), oracle_tree(cw, seed=4), keys=("tokens", "count", "path"))
     assert excused <= 2, excused
     print("ok", excused)
 
