@@ -56,7 +56,7 @@ cudaError_t launch_tree_staged(const TreeArgs& a, const StageLayout& L, int tdt,
 
 // Position-parallel chain kernel (small batches): workspace bytes and launch.
 size_t spec_workspace_bytes(int B, int K, int V, int G);
-size_t spec_smem_bytes(int V, int K, int G, int tsz, int dsz, int* t_bytes, int* d_bytes, int* fin_off);
+size_t spec_smem_bytes(int V, int G, int tsz, int dsz, int* t_bytes, int* d_bytes);
 cudaError_t launch_chain_spec(const ChainArgs& a, void* ws, int tdt, int ddt, int dk, int cluster, cudaStream_t stream);
 
 // spec_verify_chain with the workspace supplied by the library itself (used by the
