@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
             dx = (DK == DK_LOGITS) ? smem_elem<DDT>(db, x - lo) : smem_elem<DT_F32>(db, x - lo);
             has = 1;
         }
-        const PosStats ps = cluster_pos_stats(ts, ds, c, tx, dx, has, sc, phase);
+        const PosStats ps = cluster_pos_stats<DK == DK_LOGITS>(ts, ds, c, tx, dx, has, sc, phase);
         bool bad = row_bad_s(ps.t) || (DK == DK_LOGITS && k < K && row_bad_s(ps.d));
         const float inv_st = 1.f / ps.t.s;
         const float inv_sd = (DK == DK_LOGITS && k < K) ? 1.f / ps.d.s : 0.f;

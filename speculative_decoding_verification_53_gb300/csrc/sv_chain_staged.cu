@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
             if (draft_rows) dx = smem_elem<DDT>(db, x - lo);
             has = 1;
         }
-        const PosStats ps = cluster_pos_stats(ts, ds, c, tx, dx, has, sc, phase);
+        const PosStats ps = cluster_pos_stats<DK == DK_LOGITS>(ts, ds, c, tx, dx, has, sc, phase);
         if (row_bad_s(ps.t) || (draft_rows && k < K && row_bad_s(ps.d))) { invalid = true; break; }
         const float inv_st = 1.f / ps.t.s;
         if (k == K) {  // every draft accepted: bonus token from p_K

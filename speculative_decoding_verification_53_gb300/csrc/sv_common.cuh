@@ -146,6 +146,29 @@ __device__ __forceinline__ void lse_merge(LSE& a, const LSE& b, float c) {
     }
 }
 
+// Warp all-reduce of two (max, sum) pairs with their chains interleaved.
+__device__ __forceinline__ void lse2_warp_reduce(LSE& a, LSE& b, float c) {
+    float Ma = a.m, Mb = b.m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Ma = fmaxf(Ma, __shfl_xor_sync(0xffffffffu, Ma, o));
+        Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
+    }
+    float sa = (a.m > neg_inf()) ? a.s * ex2((a.m - Ma) * c) : 0.f;
+    float sb = (b.m > neg_inf()) ? b.s * ex2((b.m - Mb) * c) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sa += __shfl_xor_sync(0xffffffffu, sa, o);
+        sb += __shfl_xor_sync(0xffffffffu, sb, o);
+    }
+    a.bad = __any_sync(0xffffffffu, a.bad != 0) ? 1 : 0;
+    b.bad = __any_sync(0xffffffffu, b.bad != 0) ? 1 : 0;
+    a.m = Ma;
+    a.s = sa;
+    b.m = Mb;
+    b.s = sb;
+}
+
 __device__ __forceinline__ LSE lse_shfl_xor(const LSE& v, int mask) {
     LSE o;
     o.m = __shfl_xor_sync(0xffffffffu, v.m, mask);
@@ -301,6 +324,10 @@ __device__ __forceinline__ void dsmem_st_v4(uint32_t addr, float4 v) {
                  : "memory");
 }
 
+__device__ __forceinline__ void dsmem_st_v2(uint32_t addr, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+
 __device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
     int v;
     asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -327,6 +354,7 @@ struct WarpPart {
 struct Inbox {
     float4 part[2][MAX_CLUSTER][NW];
     float4 gath[2][MAX_CLUSTER];  // (target value, draft value, has, -) at the drafted token
+    float2 zf[2][MAX_CLUSTER];    // the draw's per-CTA total weight and failure flag
 };
 
 struct BlockScratch {
@@ -511,16 +539,14 @@ __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float*
         if (lane == 0) tile_sum[t] = s;
     }
     __syncthreads();
-    Xchg& slot = sc.xchg[phase & 1];
     if (warp == 0) {
         float z = 0.f;
         for (int t = lane; t < ntiles; t += 32) z += tile_sum[t];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        if (lane == 0) {
-            slot.f[0] = z;
-            slot.i[0] = fail_in;
-        }
+        const uint32_t Gp = cluster_size(), me = cluster_rank();
+        if ((uint32_t)lane < Gp)  // push (total, failure) into every peer's inbox
+            dsmem_st_v2(dsmem_addr(&sc.inbox.zf[phase & 1][me], (uint32_t)lane), make_float2(z, (float)fail_in));
     }
     cluster_sync_all();
     if (warp == 0) {
@@ -528,8 +554,9 @@ __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float*
         float z = 0.f;
         int fl = 0;
         if ((uint32_t)lane < G) {
-            z = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
-            fl = dsmem_ld_s32(dsmem_addr(&slot.i[0], lane));
+            const float2 v = sc.inbox.zf[phase & 1][lane];
+            z = v.x;
+            fl = v.y != 0.f ? 1 : 0;
         }
         const int any_fail = __any_sync(0xffffffffu, fl != 0) ? 1 : 0;
         float incl = z;

@@ -193,19 +193,26 @@ struct PosStats {
     int found;
 };
 
+// TWO: a draft row takes part (draft logits); otherwise only the target pair is reduced.
+template <bool TWO>
 __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, float tx, float dx, int has,
                                                       BlockScratch& sc, int& phase) {
     // Push model: lanes 0..G-1 of every warp store the warp's partials into CTA
     // `lane`'s inbox; thread 0 also pushes the values it gathered at x_k.  One
-    // cluster barrier later each CTA combines its own inbox from local memory.
+    // cluster barrier later each CTA combines its own inbox from local memory:
+    // every lane takes up to four partials, then a warp maximum, one rescale per
+    // partial and a warp sum.
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = (int)cluster_size(), me = (int)cluster_rank();
     const int buf = phase & 1;
-    lse_warp_reduce(t, c);
-    lse_warp_reduce(d, c);
+    if (TWO) {
+        lse2_warp_reduce(t, d, c);
+    } else {
+        lse_warp_reduce(t, c);
+    }
     if (lane < G) {
-        const float4 v = make_float4(t.m, t.bad ? __int_as_float(0x7fffffff) : t.s, d.m,
-                                     d.bad ? __int_as_float(0x7fffffff) : d.s);
+        const float4 v = make_float4(t.m, t.bad ? __int_as_float(0x7fffffff) : t.s, TWO ? d.m : neg_inf(),
+                                     (TWO && d.bad) ? __int_as_float(0x7fffffff) : (TWO ? d.s : 0.f));
         dsmem_st_v4(dsmem_addr(&sc.inbox.part[buf][me][warp], (uint32_t)lane), v);
     }
     if (warp == 0) {
@@ -216,26 +223,49 @@ __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, flo
     }
     cluster_sync_all();
     if (warp == 0) {
-        LSE x{neg_inf(), 0.f, 0}, y{neg_inf(), 0.f, 0};
-        for (int e = lane; e < G * NW; e += 32) {
-            const float4 v = sc.inbox.part[buf][e / NW][e % NW];
-            LSE px{v.x, v.y, v.y != v.y ? 1 : 0}, py{v.z, v.w, v.w != v.w ? 1 : 0};
-            if (px.bad) px.s = 0.f;
-            if (py.bad) py.s = 0.f;
-            lse_merge(x, px, c);
-            lse_merge(y, py, c);
+        const int E = G * NW;  // at most 16 * 8 = 128 partials: four per lane
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? sc.inbox.part[buf][e / NW][e % NW] : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
         }
-        lse_warp_reduce(x, c);
-        lse_warp_reduce(y, c);
+        float Mt = neg_inf(), Md = neg_inf();
+        int bt = 0, bd = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            Mt = fmaxf(Mt, v[i].x);
+            Md = fmaxf(Md, v[i].z);
+            bt |= v[i].y != v[i].y;
+            bd |= v[i].w != v[i].w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            Mt = fmaxf(Mt, __shfl_xor_sync(0xffffffffu, Mt, o));
+            if (TWO) Md = fmaxf(Md, __shfl_xor_sync(0xffffffffu, Md, o));
+        }
+        float St = 0.f, Sd = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (v[i].x > neg_inf() && v[i].y == v[i].y) St += v[i].y * ex2((v[i].x - Mt) * c);
+            if (TWO && v[i].z > neg_inf() && v[i].w == v[i].w) Sd += v[i].w * ex2((v[i].z - Md) * c);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            St += __shfl_xor_sync(0xffffffffu, St, o);
+            if (TWO) Sd += __shfl_xor_sync(0xffffffffu, Sd, o);
+        }
+        bt = __any_sync(0xffffffffu, bt) ? 1 : 0;
+        bd = __any_sync(0xffffffffu, bd) ? 1 : 0;
         float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
         if (lane < G) gv = sc.inbox.gath[buf][lane];
         const unsigned owners = __ballot_sync(0xffffffffu, gv.z != 0.f);
         const int src = owners ? __ffs(owners) - 1 : 0;
         const float gx = __shfl_sync(0xffffffffu, gv.x, src), gd = __shfl_sync(0xffffffffu, gv.y, src);
         if (lane == 0) {
-            sc.bf[0] = x.m; sc.bf[1] = x.s; sc.bf[2] = y.m; sc.bf[3] = y.s;
+            sc.bf[0] = Mt; sc.bf[1] = St; sc.bf[2] = TWO ? Md : neg_inf(); sc.bf[3] = TWO ? Sd : 0.f;
             sc.bf[4] = gx; sc.bf[5] = gd;
-            sc.bi[0] = x.bad; sc.bi[1] = y.bad; sc.bi[2] = owners ? 1 : 0;
+            sc.bi[0] = bt; sc.bi[1] = TWO ? bd : 0; sc.bi[2] = owners ? 1 : 0;
         }
     }
     __syncthreads();

@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
             LSE ds{neg_inf(), 0.f, 0};
             if (DK == DK_LOGITS && nchild > 0) ds = smem_thread_lse<DDT>(db, n, c);
             if (fail) ts.bad = 1;
-            const PosStats ps = cluster_pos_stats(ts, ds, c, 0.f, 0.f, 0, sc, phase);
+            const PosStats ps = cluster_pos_stats<DK == DK_LOGITS>(ts, ds, c, 0.f, 0.f, 0, sc, phase);
             if (row_bad_s(ps.t) || (DK == DK_LOGITS && nchild > 0 && row_bad_s(ps.d))) { invalid = true; break; }
             const float inv_st = 1.f / ps.t.s;
             const float inv_sd = (DK == DK_LOGITS && nchild > 0) ? 1.f / ps.d.s : 0.f;
