@@ -122,10 +122,13 @@ SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt,
  * deployment convenience).  For callers that cannot hand the library a workspace:
  * code running inside a runtime that owns every device allocation (an engine's
  * memory arena, a plugin interface that passes only input and output buffers) or a
- * path on which no allocation call is allowed.  Same arguments, outputs and results
- * as spec_verify_chain, minus the workspace: the scratch is a 2 MiB array inside
+ * path on which no allocation call is allowed.  Same arguments and outputs as
+ * spec_verify_chain, minus the workspace.  Where it applies (small batches, aligned
+ * rows) it runs the position-parallel kernel, whose scratch is a 2 MiB array inside
  * the library's device image, present on every device that loads the library until
- * the process exits.  No cudaMalloc, cudaFree or other allocating call is made.
+ * the process exits; otherwise it runs the kernels that need no scratch.  Results
+ * agree with spec_verify_chain except where a decision lies within fp32 rounding of
+ * its boundary.  No cudaMalloc, cudaFree or other allocating call is made.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress, with the device current) and zeroes it synchronously;
  *     make that first call before any stream capture.

@@ -56,7 +56,7 @@ sv_status device_info(DeviceInfo& info) {
 // Kernel-family override for comparison runs and tests: SPEC_VERIFY_PATH =
 // "spec" (position-parallel), "staged" (shared-memory staging), "stream"
 // (register streaming); anything else picks automatically.
-enum PathChoice { PATH_AUTO = 0, PATH_SPEC = 1, PATH_STAGED = 2, PATH_STREAM = 3 };
+enum PathChoice { PATH_AUTO = 0, PATH_SPEC = 1, PATH_STAGED = 2, PATH_STREAM = 3, PATH_EAGER = 4 };
 
 int path_override() {
     static int v = -1;
@@ -68,6 +68,7 @@ int path_override() {
             if (p == "spec") v = PATH_SPEC;
             if (p == "staged") v = PATH_STAGED;
             if (p == "stream") v = PATH_STREAM;
+            if (p == "eager") v = PATH_EAGER;
         }
     }
     return v;
@@ -121,11 +122,23 @@ int spec_cluster(int B, int K, int num_sms) {
 //  - shared-memory staged walk (sv_chain_staged.cu) when rows are 16-byte aligned;
 //  - register-streaming walk (sv_chain.cu) otherwise.
 sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_draft, int num_sms, void* ws,
-                    size_t ws_bytes, cudaStream_t stream) {
-    const int path = path_override();
+                    size_t ws_bytes, cudaStream_t stream, int forced_path = PATH_AUTO) {
+    const int path = forced_path != PATH_AUTO ? forced_path : path_override();
     const size_t tsz = dtype_size(tdt), dsz = dk == SV_DRAFT_PROBS ? 4 : dtype_size(ddt);
     const bool aligned = aligned16(a.target) && (a.V * tsz) % 16 == 0 &&
                          (!uses_draft || (aligned16(a.draft) && (a.V * dsz) % 16 == 0));
+    // all positions staged at once, one cluster per row (only when requested: measured slower
+    // than the position-parallel kernel at B = 1, 14.2 against 9.4 us)
+    if (path == PATH_EAGER && aligned && a.K + 1 <= 16) {
+        int Ge = 16;
+        while (Ge > 1 && (long long)a.B * Ge > num_sms) Ge >>= 1;
+        {
+            const cudaError_t e = sv::launch_chain_eager(a, tdt, ddt, dk, Ge, stream);
+            if (e == cudaSuccess) return SV_OK;
+            if (e != cudaErrorInvalidClusterSize) return launch_status(e);
+            (void)cudaGetLastError();
+        }
+    }
     if ((path == PATH_AUTO || path == PATH_SPEC) && aligned && ws && ((uintptr_t)ws & 255u) == 0) {
         const int Gs = spec_cluster(a.B, a.K, num_sms);
         if ((path == PATH_SPEC || Gs >= 4) && ws_bytes >= sv::spec_workspace_bytes(a.B, a.K, a.V, Gs)) {
@@ -155,9 +168,21 @@ sv_status chain_with_scratch(const void* target_logits, int tdt, const void* dra
                              const int32_t* draft_tokens, const float* temperature, int B, int K, int V,
                              uint64_t seed, uint64_t offset, int32_t* out_tokens, int32_t* out_count,
                              float* out_accept_prob, void* scratch, size_t scratch_bytes, void* stream) {
-    return spec_verify_chain(target_logits, (sv_dtype)tdt, draft, (sv_dtype)ddt, (sv_draft_kind)dk, draft_tokens,
-                             temperature, B, K, V, seed, offset, out_tokens, out_count, out_accept_prob, scratch,
-                             scratch_bytes, stream);
+    // same checks as spec_verify_chain; the position-parallel kernel (the one that uses the
+    // scratch) is taken whenever it applies, the scratch-free kernels otherwise
+    if (B < 0 || B > kMaxB || K < 0 || K > kMaxK || V < 1 || V > kMaxV) return SV_ERR_INVALID_ARG;
+    if (!is_dtype(tdt) || !is_dtype(ddt)) return SV_ERR_INVALID_ARG;
+    if (dk != SV_DRAFT_PROBS && dk != SV_DRAFT_LOGITS) return SV_ERR_INVALID_ARG;
+    if (dk == SV_DRAFT_PROBS && ddt != SV_F32) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !temperature || !out_tokens || !out_count || (K > 0 && (!draft_tokens || !draft)))
+        return SV_ERR_INVALID_ARG;
+    DeviceInfo info;
+    sv_status st = device_info(info);
+    if (st != SV_OK) return st;
+    ChainArgs a{target_logits, draft, draft_tokens, temperature, B, K, V, seed, offset,
+                out_tokens, out_count, out_accept_prob};
+    return run_chain(a, tdt, ddt, dk, K > 0, info.sms, scratch, scratch_bytes, (cudaStream_t)stream, PATH_SPEC);
 }
 
 int choose_cluster(int B, int V, int num_sms) {

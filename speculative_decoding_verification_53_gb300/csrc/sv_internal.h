@@ -54,6 +54,9 @@ cudaError_t launch_chain_staged(const ChainArgs& a, const StageLayout& L, int td
 cudaError_t launch_tree_staged(const TreeArgs& a, const StageLayout& L, int tdt, int ddt, int dk, int cluster,
                                cudaStream_t stream);
 
+// All-positions-at-once chain kernel (small batches, K + 1 <= 16).
+cudaError_t launch_chain_eager(const ChainArgs& a, int tdt, int ddt, int dk, int cluster, cudaStream_t stream);
+
 // Position-parallel chain kernel (small batches): workspace bytes and launch.
 size_t spec_workspace_bytes(int B, int K, int V, int G);
 size_t spec_smem_bytes(int V, int G, int tsz, int dsz, int* t_bytes, int* d_bytes);
