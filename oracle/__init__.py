@@ -63,8 +63,11 @@ def _load():
                                              f64p, f64p, i32p, i32p, i32p, f64p]
         lib.oracle_verify_tree.argtypes = [vp, ci, vp, ci, ci, i32p, i32p, f32p, ci, ci, ci, ci,
                                            u64, u64, i32p, i32p, i32p, i32p, f64p]
+        lib.oracle_tree_mask.argtypes = [i32p, ci, ci, vp, i32p, i32p]
+        lib.oracle_kv_compact.argtypes = [vp, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t, i32p, i32p, i32p,
+                                          ci, ci, ci]
         for name in ("oracle_verify_chain_u", "oracle_verify_chain", "oracle_greedy_accept",
-                     "oracle_verify_tree_u", "oracle_verify_tree"):
+                     "oracle_verify_tree_u", "oracle_verify_tree", "oracle_tree_mask", "oracle_kv_compact"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -203,3 +206,33 @@ def verify_tree(target, draft, node_tokens, parent, temperature, max_depth, seed
                                      _ptr(out_t, ctypes.c_int32), _ptr(out_c, ctypes.c_int32),
                                      _ptr(out_p, ctypes.c_int32), _ptr(out_m, ctypes.c_double))
     return dict(tokens=out_t, count=out_c, path=out_p[:, :D], margin=out_m, n_invalid=n)
+
+
+def tree_mask(parent):
+    """Ancestor-or-self bitmask of each node: parent [B][N] -> (mask uint32 [B][N][W],
+    depth int32 [B][N], valid int32 [B])."""
+    lib = _load()
+    par = _c(parent, np.int32)
+    B, N = par.shape
+    W = (N + 31) // 32
+    mask = np.zeros((B, N, W), np.uint32)
+    depth = np.zeros((B, N), np.int32)
+    valid = np.zeros(B, np.int32)
+    lib.oracle_tree_mask(_ptr(par, ctypes.c_int32), B, N, mask.ctypes.data, _ptr(depth, ctypes.c_int32),
+                         _ptr(valid, ctypes.c_int32))
+    return dict(mask=mask, depth=depth, valid=valid)
+
+
+def kv_compact(kv, path, count, base):
+    """Accepted-path KV compaction on a copy of kv [B][R][row_bytes] (uint8):
+    row base+d <- row base+path[d] for d < count-1, in order.  Returns the new cache."""
+    lib = _load()
+    out = np.array(kv, dtype=np.uint8, copy=True, order="C")
+    B, R, rb = out.shape
+    pth = _c(path, np.int32)
+    D = pth.shape[1]
+    cnt = _c(count, np.int32)
+    bs = _c(base, np.int32)
+    lib.oracle_kv_compact(out.ctypes.data, R * rb, rb, rb, _ptr(pth, ctypes.c_int32), _ptr(cnt, ctypes.c_int32),
+                          _ptr(bs, ctypes.c_int32), B, D, R)
+    return out

@@ -453,3 +453,78 @@ int oracle_verify_tree(const void *target, int tdt, const void *draft, int ddt, 
     free(u);
     return n;
 }
+
+/* ------------------------------------------------------ tree attention mask */
+
+/*
+ * Ancestor-or-self mask of a draft tree ("Speculative Decoding and EAGLE", section
+ * "트리 어텐션 검증": each node attends only to its ancestors in the tree; the node
+ * itself is included, as causal attention always includes the current token;
+ * "Progressive Tree Drafting", section "트리 구조 드래프팅": the attention mask is
+ * rebuilt so one forward pass follows every branch).
+ *  parent [B][N] with parent[i] in {-1} u [0, i).  mask [B][N][W], W = (N+31)/32,
+ *  bit j of row i set iff j is i or an ancestor of i.  depth [B][N]: nodes on the
+ *  path from the root's child down to i (1 for a child of the root).  valid [B]:
+ *  1, or 0 for a malformed parent array (its mask rows and depths are then 0).
+ */
+int oracle_tree_mask(const int32_t *parent, int B, int N, uint32_t *mask, int32_t *depth, int32_t *valid)
+{
+    const int W = (N + 31) / 32;
+    int n_invalid = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parent + (size_t)b * N;
+        uint32_t *m = mask + (size_t)b * N * W;
+        int32_t *dp = depth + (size_t)b * N;
+        int ok = 1;
+        for (int i = 0; i < N; ++i)
+            if (par[i] < -1 || par[i] >= i) ok = 0;
+        memset(m, 0, sizeof(uint32_t) * (size_t)N * W);
+        for (int i = 0; i < N; ++i) dp[i] = 0;
+        if (ok) {
+            for (int i = 0; i < N; ++i) {
+                int d = 0;
+                for (int j = i; j >= 0; j = par[j]) {  /* walk up to the root */
+                    m[(size_t)i * W + j / 32] |= 1u << (j % 32);
+                    ++d;
+                }
+                dp[i] = d;
+            }
+        } else {
+            ++n_invalid;
+        }
+        valid[b] = ok;
+    }
+    return n_invalid;
+}
+
+/* --------------------------------------------------- accepted-path KV compaction */
+
+/*
+ * KV-cache rollback after a tree verify (the velog review of Leviathan et al.,
+ * section 4 "한계점": the KV entries of rejected tokens must be rolled back).  Tree
+ * node i's cache row sits at base[b] + i; the accepted nodes path[0..L-1]
+ * (L = count - 1: the last emitted token has no cache row yet) are moved, in order,
+ * to rows base[b] + 0..L-1: for d = 0..L-1, row base+d <- row base+path[d].
+ * kv: bytes, row r of batch row b at b*batch_stride + r*row_stride, row_bytes each.
+ * A batch row whose count is 0 or above D + 1, whose path has an entry path[d] < d,
+ * or whose rows fall outside [0, num_rows) is left untouched.  (With path[d] >= d no
+ * step reads a row an earlier step wrote, so the in-order copy equals a gather from
+ * the cache as it was before the call.)
+ */
+int oracle_kv_compact(unsigned char *kv, size_t batch_stride, size_t row_stride, size_t row_bytes,
+                      const int32_t *path, const int32_t *count, const int32_t *base, int B, int D, int num_rows)
+{
+    int skipped = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *pth = path + (size_t)b * D;
+        const int L = count[b] - 1;
+        int ok = count[b] >= 1 && L <= D;
+        for (int d = 0; ok && d < L; ++d)
+            if (pth[d] < d || base[b] < 0 || base[b] + pth[d] >= num_rows) ok = 0;
+        if (!ok) { ++skipped; continue; }
+        unsigned char *rowb = kv + (size_t)b * batch_stride;
+        for (int d = 0; d < L; ++d)
+            memmove(rowb + (size_t)(base[b] + d) * row_stride, rowb + (size_t)(base[b] + pth[d]) * row_stride, row_bytes);
+    }
+    return skipped;
+}

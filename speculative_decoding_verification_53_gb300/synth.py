@@ -275,3 +275,70 @@ def redraw_tokens(w: dict, temperature: float, seed: int) -> dict:
     out["tokens"] = tokens
     out["temperature"] = np.full(B, temperature, np.float32)
     return out
+
+
+# ------------------------------------------------------------ tree shapes and KV caches
+
+def random_parents(seed: int, B: int, N: int, shape: str = "bfs", branch: int = 3,
+                   max_depth: int = 6) -> np.ndarray:
+    """Parent arrays [B][N] with parent[i] in {-1} u [0, i).
+
+    shape: "bfs"    breadth-first tree, up to ``branch`` children a node and depth
+                    <= ``max_depth`` (the draft-tree shape), a random fan-out per node;
+           "random" parent[i] uniform over {-1, 0, .., i-1} (deep, irregular);
+           "chain"  parent[i] = i - 1;  "star"  every node a child of the root."""
+    out = np.empty((B, N), np.int32)
+    for b in range(B):
+        rng = np.random.default_rng([seed, b, 7])
+        if shape == "chain":
+            out[b] = np.arange(-1, N - 1)
+        elif shape == "star":
+            out[b] = -1
+        elif shape == "random":
+            out[b] = [int(rng.integers(-1, i)) if i > 0 else -1 for i in range(N)]
+        else:
+            par, depth = [], []
+            frontier = [(-1, 0)]          # (node, depth); -1 is the root
+            head = 0
+            while len(par) < N:
+                if head >= len(frontier):  # every node at max depth: restart at the root
+                    frontier.append((-1, 0))
+                node, d = frontier[head]
+                head += 1
+                if d >= max_depth:
+                    continue
+                for _ in range(int(rng.integers(1, branch + 1))):
+                    if len(par) == N:
+                        break
+                    par.append(node)
+                    depth.append(d + 1)
+                    frontier.append((len(par) - 1, d + 1))
+            out[b] = par
+    return out
+
+
+def accepted_paths(seed: int, parent: np.ndarray, max_depth: int):
+    """A tree-verify-shaped result for each batch row: a random node's root-to-node
+    path (node indices, -1 padded to ``max_depth``) and count = path length + 1.
+    Rows whose chosen node is deeper than ``max_depth`` take its ancestor at that depth."""
+    B, N = parent.shape
+    path = np.full((B, max_depth), -1, np.int32)
+    count = np.empty(B, np.int32)
+    for b in range(B):
+        rng = np.random.default_rng([seed, b, 11])
+        chain = []
+        j = int(rng.integers(-1, N))     # -1: nothing accepted
+        while j >= 0:
+            chain.append(j)
+            j = int(parent[b, j])
+        chain = chain[::-1][:max_depth]
+        path[b, :len(chain)] = chain
+        count[b] = len(chain) + 1
+    return path, count
+
+
+def kv_cache(seed: int, n_buffers: int, B: int, planes: int, rows: int, row_bytes: int) -> np.ndarray:
+    """Random bytes shaped [n_buffers][B][planes][rows][row_bytes] (one buffer per
+    layer and K/V; a plane is a KV head; a row is one token's head vector)."""
+    rng = np.random.default_rng([seed, 13])
+    return rng.integers(0, 256, (n_buffers, B, planes, rows, row_bytes), dtype=np.uint8)
