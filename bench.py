@@ -10,7 +10,11 @@ through them; steps are replayed from CUDA graphs so that host launch gaps do
 not enter the device timing.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--workload single_stream|large_batch|mixed_batch|tree]
+                  [--workload single_stream|large_batch|mixed_batch|tree|tree_mask|kv_compact]
+
+tree_mask and kv_compact time the steps on either side of a tree verify (the
+ancestor attention mask of each draft tree; moving the accepted branch's KV-cache
+rows to the front) with their own metric and unit.
 
 Prints one JSON line (rank 0).  `value` is verify rows/s over all ranks;
 `roofline` relates the kernel's algorithmic bytes per launch (the rows the rule
@@ -487,6 +491,257 @@ def run_reference(args, rank):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------ steps around a tree verify
+
+AUX_WORKLOADS = ("tree_mask", "kv_compact")
+KV_LAYOUT = dict(n_buffers=64, heads=8, rows=1024, dim=128, nodes=60, depth=6, sets=16)
+
+
+def make_aux(args, rank):
+    from speculative_decoding_verification_53_gb300 import synth
+    seed = 2000 + rank
+    if args.workload == "tree_mask":
+        B = args.batch or 1024
+        N = args.nodes or 1024
+        par = synth.random_parents(seed, B, N, shape="bfs", branch=3, max_depth=6 if N <= 64 else 16)
+        W = (N + 31) // 32
+        return dict(parent=par, B=B, N=N, W=W, metric=f"tree-attention masks/s (N={N}-node draft trees)",
+                    unit="trees/s", per_step=B,
+                    bytes_per_step=B * N * 4 + B * N * W * 4 + B * N * 4 + B * 4,
+                    desc=f"tree-attention mask, B={B} trees of N={N} nodes (breadth-first, up to 3 children, "
+                         f"depth<={6 if N <= 64 else 16}), uint32 ancestor bitmask [B][N][{W}] + depth")
+    L = dict(KV_LAYOUT)
+    B = args.batch or 32
+    par = synth.random_parents(seed, B * L["sets"], L["nodes"], max_depth=L["depth"])
+    path, count = synth.accepted_paths(seed, par, L["depth"])
+    base = np.repeat(np.arange(L["sets"], dtype=np.int32) * (L["rows"] // L["sets"]), B)
+    moves = np.array([sum(1 for d in range(c - 1) if p[d] != d) for p, c in zip(path, count)])
+    row_bytes = L["dim"] * 2
+    per_set = moves.reshape(L["sets"], B).sum(1) * 2 * row_bytes * L["heads"] * L["n_buffers"]
+    return dict(path=path, count=count, base=base, B=B, layout=L, per_step=B,
+                metric="accepted-path KV compactions/s (batch rows, every layer's K and V)", unit="batch rows/s",
+                bytes_per_set=per_set, row_bytes=row_bytes,
+                desc=f"accepted-path KV compaction, B={B}, {L['n_buffers']} cache tensors (32 layers x K,V) of "
+                     f"[B][{L['heads']} heads][{L['rows']} rows][{L['dim']}] bf16, tree of {L['nodes']} nodes, "
+                     f"depth<={L['depth']}, {L['sets']} resident path sets in disjoint row windows")
+
+
+def run_aux(args, rank, world, device):
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    from speculative_decoding_verification_53_gb300 import build as svbuild
+    if rank == 0:
+        svbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    sv.lib()
+    a = make_aux(args, rank)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+    chunk = min(args.steps, 1000)
+    if args.workload == "tree_mask":
+        dpar = torch.from_numpy(a["parent"]).to(device)
+        outs = [(torch.empty((a["B"], a["N"], a["W"]), dtype=torch.int32, device=device),
+                 torch.empty((a["B"], a["N"]), dtype=torch.int32, device=device),
+                 torch.empty((a["B"],), dtype=torch.int32, device=device)) for _ in range(2)]
+
+        def step(i):
+            m, d, v = outs[i % 2]
+            sv.spec_tree_mask(dpar, out_mask=m, out_depth=d, out_valid=v)
+
+        def bytes_of(i):
+            return a["bytes_per_step"]
+        l2 = "outputs of two alternating steps (2 x %.0f MB) larger than L2" % (a["B"] * a["N"] * a["W"] * 4 / 1e6)
+        kernel = "tree_mask_kernel"
+    else:
+        L = a["layout"]
+        kv = torch.empty((L["n_buffers"], a["B"], L["heads"], L["rows"], L["dim"]), dtype=torch.bfloat16,
+                         device=device)
+        kv.fill_(1.0)
+        bufs = [kv[k] for k in range(L["n_buffers"])]
+        a["bufs"] = bufs
+        dpath = torch.from_numpy(a["path"]).to(device)
+        dcount = torch.from_numpy(a["count"]).to(device)
+        dbase = torch.from_numpy(a["base"]).to(device)
+        B = a["B"]
+
+        def step(i):
+            s = i % L["sets"]
+            sl = slice(s * B, (s + 1) * B)
+            sv.spec_kv_compact(bufs, dpath[sl], dcount[sl], dbase[sl])
+
+        def bytes_of(i):
+            return float(a["bytes_per_set"][i % L["sets"]])
+        l2 = f"{L['sets']} path sets in disjoint cache windows cycled (touched bytes per cycle > L2)"
+        kernel = "kv_compact_kernel"
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize(device)
+    reps, rem = divmod(args.steps, chunk)
+    graphs = []
+    for n in ([chunk] if reps else []) + ([rem] if rem else []):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        graphs.append((g, n))
+    for g, _ in graphs:
+        g.replay()
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        t_wall = time.time()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+        start.record(stream)
+        for _ in range(reps):
+            graphs[0][0].replay()
+        if rem:
+            graphs[-1][0].replay()
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        if world > 1:
+            torch.distributed.barrier()
+        elapsed_ms = start.elapsed_time(end)
+        while time.time() - t_wall < 1.5:
+            graphs[0][0].replay()
+            torch.cuda.synchronize(device)
+    clock = clocks.summary()
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    max_ms = float(t.item())
+    ms_per_step = max_ms / args.steps
+    value = a["per_step"] * args.steps * world / (max_ms / 1e3)
+    bytes_per_launch = float(np.mean([bytes_of(i) for i in range(chunk)]))
+    e2e = run_aux_e2e(args, a, device, stream)
+    cpu = run_aux_cpu(args, a, budget_s=10.0) if (rank == 0 and not args.no_cpu_baseline) else None
+    if rank != 0:
+        return None
+    peak, peak_src = measured_peak()
+    achieved = bytes_per_launch / (ms_per_step / 1e3) / 1e9
+    traffic, prof, prof_kernel = profile_traffic(args.workload)
+    return {
+        "metric": a["metric"], "value": value, "unit": a["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32" if args.workload == "tree_mask" else "u8", "data": "synthetic",
+        "config": {"workload": a["desc"], "batch_rows_per_step": a["per_step"], "l2": l2,
+                   "timing": "CUDA-graph replay, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (STREAM copy)",
+                     "algorithmic_bytes_per_launch": bytes_per_launch, "kernel": prof_kernel or kernel,
+                     "traffic_source": prof},
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps, "clocks": clock,
+    }
+
+
+def run_aux_e2e(args, a, device, stream):
+    """Through the public API with host buffers: the inputs copied in and the result
+    read back every step (the mask and depths; for the compaction the counts, the cache
+    itself being device state)."""
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    n = min(args.e2e_steps, max(args.steps, 3))
+    if args.workload == "tree_mask":
+        hpar = torch.from_numpy(a["parent"]).pin_memory()
+        dpar = torch.empty_like(hpar, device=device)
+        hm = torch.empty((a["B"], a["N"], a["W"]), dtype=torch.int32).pin_memory()
+        hd = torch.empty((a["B"], a["N"]), dtype=torch.int32).pin_memory()
+        h2d, d2h = hpar.numel() * 4, hm.numel() * 4 + hd.numel() * 4
+
+        def one(i):
+            dpar.copy_(hpar, non_blocking=True)
+            m, d, _ = sv.spec_tree_mask(dpar)
+            hm.copy_(m, non_blocking=True)
+            hd.copy_(d, non_blocking=True)
+    else:
+        B = a["B"]
+        bufs = a["bufs"]
+        hp = torch.from_numpy(a["path"][:B]).pin_memory()
+        hc = torch.from_numpy(a["count"][:B]).pin_memory()
+        hb = torch.from_numpy(a["base"][:B]).pin_memory()
+        dp, dc, db = (torch.empty_like(x, device=device) for x in (hp, hc, hb))
+        ho = torch.empty_like(hc).pin_memory()
+        h2d, d2h = (hp.numel() + hc.numel() + hb.numel()) * 4, ho.numel() * 4
+
+        def one(i):
+            dp.copy_(hp, non_blocking=True)
+            dc.copy_(hc, non_blocking=True)
+            db.copy_(hb, non_blocking=True)
+            sv.spec_kv_compact(bufs, dp, dc, db)
+            ho.copy_(dc, non_blocking=True)
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(n):
+        one(i)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    ms = start.elapsed_time(end)
+    return {"value": a["per_step"] * n / (ms / 1e3), "unit": a["unit"], "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": ms / n}
+
+
+def _aux_oracle_loop(a, workload, budget_s, max_steps=None):
+    """Runs the oracle on successive steps of the workload until the budget (or
+    max_steps) is spent; returns (steps, units, seconds, sample text)."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    steps = units = 0
+    if workload == "tree_mask":
+        while time.perf_counter() - t0 < budget_s and (max_steps is None or steps < max_steps):
+            oracle.tree_mask(a["parent"])
+            steps += 1
+            units += a["B"]
+        return steps, units, time.perf_counter() - t0, f"{steps} full steps ({units} trees)"
+    L = a["layout"]
+    B = a["B"]
+    # one cache tensor at a time: [B*heads][rows][row_bytes], compacted in place
+    cache = np.zeros((B * L["heads"], L["rows"], a["row_bytes"]), np.uint8)
+    t0 = time.perf_counter()
+    tensors = 0
+    while time.perf_counter() - t0 < budget_s and (max_steps is None or steps < max_steps):
+        s = (tensors // L["n_buffers"]) % L["sets"]
+        sl = slice(s * B, (s + 1) * B)
+        oracle.kv_compact(cache, np.repeat(a["path"][sl], L["heads"], axis=0), np.repeat(a["count"][sl], L["heads"]),
+                          np.repeat(a["base"][sl], L["heads"]), inplace=True)
+        tensors += 1
+        if tensors % L["n_buffers"] == 0:
+            steps += 1
+    el = time.perf_counter() - t0
+    units = B * tensors / L["n_buffers"]
+    return steps, units, el, f"{tensors} cache tensors ({tensors / L['n_buffers']:.1f} steps)"
+
+
+def run_aux_cpu(args, a, budget_s=10.0):
+    steps, units, el, sample = _aux_oracle_loop(a, args.workload, budget_s)
+    return {"value": units / el, "unit": a["unit"], "cores": 1, "kind": "oracle",
+            "sample": f"{sample} of the same workload in {el:.1f} s, single thread"}
+
+
+def run_aux_reference(args, rank):
+    if rank != 0:
+        return None
+    a = make_aux(args, 0)
+    steps, units, el, sample = _aux_oracle_loop(a, args.workload, 120.0, max_steps=args.steps)
+    value = units / el
+    return {"metric": a["metric"], "value": value, "unit": a["unit"], "n_gpus": args.gpus, "steps": steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": el / max(steps, 1) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u32" if args.workload == "tree_mask" else "u8",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": a["desc"], "batch_rows_per_step": a["per_step"], "steps_requested": args.steps,
+                       "time_budget_s": 120.0},
+            "cpu_baseline": {"value": value, "unit": a["unit"], "cores": 1, "kind": "oracle",
+                             "sample": f"{sample} on one host core (C oracle)"},
+            "e2e": {"value": value, "unit": a["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 # -------------------------------------------------------------------- main
 
 def main():
@@ -496,10 +751,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="single_stream",
-                    choices=["single_stream", "large_batch", "mixed_batch", "tree"])
+                    choices=["single_stream", "large_batch", "mixed_batch", "tree", "tree_mask", "kv_compact"])
     ap.add_argument("--rounds", type=int, default=64, help="resident rounds of the single-stream workload")
     ap.add_argument("--e2e-steps", type=int, default=300)
-    ap.add_argument("--batch", type=int, default=0, help="batch rows of the large-batch workload (default 256)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="batch rows (large_batch: 256, tree_mask: 1024 trees, kv_compact: 32)")
+    ap.add_argument("--nodes", type=int, default=0, help="tree nodes of the tree_mask workload (default 1024)")
     ap.add_argument("--temperature", type=float, default=None, help="temperature of the large-batch workload")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     args = ap.parse_args()
@@ -507,8 +764,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
+    aux = args.workload in AUX_WORKLOADS
     if args.impl == "reference":
-        line = run_reference(args, rank)
+        line = run_aux_reference(args, rank) if aux else run_reference(args, rank)
         if line is not None:
             print(json.dumps(line), flush=True)
         return
@@ -518,7 +776,7 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    line = run_ours(args, rank, world, device)
+    line = run_aux(args, rank, world, device) if aux else run_ours(args, rank, world, device)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -223,11 +223,17 @@ def tree_mask(parent):
     return dict(mask=mask, depth=depth, valid=valid)
 
 
-def kv_compact(kv, path, count, base):
-    """Accepted-path KV compaction on a copy of kv [B][R][row_bytes] (uint8):
-    row base+d <- row base+path[d] for d < count-1, in order.  Returns the new cache."""
+def kv_compact(kv, path, count, base, inplace=False):
+    """Accepted-path KV compaction of kv [B][R][row_bytes] (uint8): row base+d <- row
+    base+path[d] for d < count-1, in order.  Works on a copy (returned) unless
+    ``inplace`` (kv must then be a C-contiguous uint8 array; it is returned)."""
     lib = _load()
-    out = np.array(kv, dtype=np.uint8, copy=True, order="C")
+    if inplace:
+        if kv.dtype != np.uint8 or not kv.flags["C_CONTIGUOUS"]:
+            raise ValueError("in-place compaction needs a C-contiguous uint8 array")
+        out = kv
+    else:
+        out = np.array(kv, dtype=np.uint8, copy=True, order="C")
     B, R, rb = out.shape
     pth = _c(path, np.int32)
     D = pth.shape[1]

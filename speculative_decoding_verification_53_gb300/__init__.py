@@ -23,7 +23,8 @@ SV_F32, SV_BF16 = 0, 1
 SV_DRAFT_PROBS, SV_DRAFT_LOGITS = 0, 1
 
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_chain", "spec_greedy_accept", "spec_verify_tree",
-           "spec_verify_status_string", "spec_verify_last_cuda_error", "spec_verify_chain_noalloc")
+           "spec_verify_status_string", "spec_verify_last_cuda_error", "spec_verify_chain_noalloc",
+           "spec_tree_mask", "spec_kv_compact")
 
 _lib = None
 
@@ -57,6 +58,11 @@ def lib() -> ctypes.CDLL:
     L.spec_greedy_accept.restype = ci
     L.spec_verify_tree.argtypes = [vp, ci, vp, ci, ci, vp, vp, vp, ci, ci, ci, ci, u64, u64, vp, vp, vp, vp]
     L.spec_verify_tree.restype = ci
+    L.spec_tree_mask.argtypes = [vp, ci, ci, vp, vp, vp, vp]
+    L.spec_tree_mask.restype = ci
+    i64 = ctypes.c_int64
+    L.spec_kv_compact.argtypes = [ctypes.POINTER(vp), ci, i64, i64, ci, i64, i64, ci, vp, vp, vp, ci, ci, vp]
+    L.spec_kv_compact.restype = ci
     L.spec_verify_status_string.argtypes = [ci]
     L.spec_verify_status_string.restype = ctypes.c_char_p
     L.spec_verify_last_cuda_error.argtypes = []
@@ -257,3 +263,55 @@ def spec_verify_tree(target_logits, draft, node_tokens, parent, temperature, max
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_tree")
     return out_tokens, out_count, out_path
+
+
+def spec_tree_mask(parent, *, out_mask=None, out_depth=None, out_valid=None, stream=None):
+    """Ancestor-or-self attention mask of each draft tree.  parent int32 [B][N].
+    Returns (out_mask int32 [B][N][ceil(N/32)] holding the uint32 bit words, out_depth
+    int32 [B][N], out_valid int32 [B])."""
+    torch = _torch()
+    _dev(parent, "parent", torch.int32)
+    B, N = parent.shape
+    W = (N + 31) // 32
+    dev = parent.device
+    if out_mask is None:
+        out_mask = torch.empty((B, N, W), dtype=torch.int32, device=dev)
+    if out_depth is None:
+        out_depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if out_valid is None:
+        out_valid = torch.empty((B,), dtype=torch.int32, device=dev)
+    st = lib().spec_tree_mask(_ptr(parent), B, N, _ptr(out_mask), _ptr(out_depth), _ptr(out_valid),
+                              _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_tree_mask")
+    return out_mask, out_depth, out_valid
+
+
+def spec_kv_compact(kv_buffers, path, count, base=None, *, stream=None):
+    """Move each batch row's accepted tree nodes' cache rows to the front, in place.
+    kv_buffers: CUDA tensors of one dtype and identical shape [B][planes][rows][width]
+    and strides (any strided view whose last dimension is contiguous, e.g. a
+    [B][rows][heads][dim] cache permuted to [B][heads][rows][dim]).  path int32
+    [B][D] and count int32 [B] as spec_verify_tree returns them; base int32 [B] (the
+    cache row of tree node 0) or None for 0."""
+    torch = _torch()
+    bufs = list(kv_buffers)
+    if not bufs:
+        raise ValueError("kv_buffers is empty")
+    t0 = bufs[0]
+    for t in bufs:
+        if not t.is_cuda or t.dim() != 4 or t.shape != t0.shape or t.stride() != t0.stride() or t.dtype != t0.dtype:
+            raise ValueError("kv_buffers must be CUDA tensors [B][planes][rows][width] of one shape, stride and dtype")
+        if t.stride(3) != 1:
+            raise ValueError("the last dimension of every kv buffer must be contiguous")
+    _dev(path, "path", torch.int32)
+    _dev(count, "count", torch.int32)
+    _dev(base, "base", torch.int32)
+    B, H, R, Wd = t0.shape
+    es = t0.element_size()
+    arr = (ctypes.c_void_p * len(bufs))(*[t.data_ptr() for t in bufs])
+    st = lib().spec_kv_compact(arr, len(bufs), t0.stride(0) * es, t0.stride(1) * es, H, t0.stride(2) * es,
+                               Wd * es, R, _ptr(path), _ptr(count), _ptr(base), B, path.shape[1],
+                               _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_kv_compact")

@@ -6,6 +6,22 @@
 #include "spec_verify.h"
 #include "sv_internal.h"
 
+namespace sv {
+
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+sv_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return SV_OK;
+    g_last_cuda_error = e;
+    (void)cudaGetLastError();
+    return SV_ERR_CUDA;
+}
+
+}  // namespace sv
+
+using sv::g_last_cuda_error;
+using sv::launch_status;
+
 namespace {
 
 constexpr int kMaxK = 64;
@@ -26,15 +42,6 @@ int cluster_override() {
 }
 
 bool is_dtype(int d) { return d == SV_F32 || d == SV_BF16; }
-
-thread_local cudaError_t g_last_cuda_error = cudaSuccess;
-
-sv_status launch_status(cudaError_t e) {
-    if (e == cudaSuccess) return SV_OK;
-    g_last_cuda_error = e;
-    (void)cudaGetLastError();
-    return SV_ERR_CUDA;
-}
 
 struct DeviceInfo {
     int sms = 0;

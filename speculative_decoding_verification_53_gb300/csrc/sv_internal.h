@@ -10,6 +10,10 @@
 
 namespace sv {
 
+// Records a CUDA error for spec_verify_last_cuda_error (per calling thread), clears
+// the sticky launch error and returns SV_ERR_CUDA; cudaSuccess gives SV_OK.
+sv_status launch_status(cudaError_t e);
+
 struct ChainArgs {
     const void* target;        // [B][K+1][V]
     const void* draft;         // [B][K][V] probs (fp32) or logits
