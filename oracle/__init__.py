@@ -63,11 +63,16 @@ def _load():
                                              f64p, f64p, i32p, i32p, i32p, f64p]
         lib.oracle_verify_tree.argtypes = [vp, ci, vp, ci, ci, i32p, i32p, f32p, ci, ci, ci, ci,
                                            u64, u64, i32p, i32p, i32p, i32p, f64p]
+        lib.oracle_verify_tree_rule_u.argtypes = [vp, ci, vp, ci, ci, i32p, i32p, f32p, ci, ci, ci, ci, ci,
+                                                  f64p, f64p, i32p, i32p, i32p, f64p]
+        lib.oracle_verify_tree_rule.argtypes = [vp, ci, vp, ci, ci, i32p, i32p, f32p, ci, ci, ci, ci, ci,
+                                                u64, u64, i32p, i32p, i32p, i32p, f64p]
         lib.oracle_tree_mask.argtypes = [i32p, ci, ci, vp, i32p, i32p]
         lib.oracle_kv_compact.argtypes = [vp, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t, i32p, i32p, i32p,
                                           ci, ci, ci]
         for name in ("oracle_verify_chain_u", "oracle_verify_chain", "oracle_greedy_accept",
-                     "oracle_verify_tree_u", "oracle_verify_tree", "oracle_tree_mask", "oracle_kv_compact"):
+                     "oracle_verify_tree_u", "oracle_verify_tree", "oracle_tree_mask", "oracle_kv_compact",
+                     "oracle_verify_tree_rule_u", "oracle_verify_tree_rule"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -164,11 +169,16 @@ def greedy_accept(target, draft_tokens):
     return dict(tokens=out_t, count=out_c, n_invalid=n)
 
 
+SIBLINGS_WOR, SIBLINGS_IID = 0, 1
+
+
 def verify_tree(target, draft, node_tokens, parent, temperature, max_depth, seed, offset,
-                draft_kind=DRAFT_LOGITS, row_id=None, uniforms=None):
+                draft_kind=DRAFT_LOGITS, row_id=None, uniforms=None, sibling_rule=SIBLINGS_WOR):
     """Tree verify.  target/draft [B][N+1][V] (row 0 = root, row i+1 = after node i),
     node_tokens/parent [B][N].  ``uniforms=(r, u)`` ([B][N], [B][N+1]) replaces the
-    Philox stream.  Returns dict(tokens, count, path, margin, n_invalid)."""
+    Philox stream.  sibling_rule: SIBLINGS_WOR (siblings drafted without replacement:
+    a rejected token's q is zeroed and q renormalised) or SIBLINGS_IID (drafted
+    i.i.d.: q unchanged).  Returns dict(tokens, count, path, margin, n_invalid)."""
     lib = _load()
     target = np.ascontiguousarray(target)
     B, N1, V = target.shape
@@ -189,9 +199,9 @@ def verify_tree(target, draft, node_tokens, parent, temperature, max_depth, seed
     dptr = None if draft is None else draft.ctypes.data
     if uniforms is None:
         rid = None if row_id is None else _c(row_id, np.int32)
-        n = lib.oracle_verify_tree(target.ctypes.data, tdt, dptr, ddt, draft_kind,
+        n = lib.oracle_verify_tree_rule(target.ctypes.data, tdt, dptr, ddt, draft_kind,
                                    _ptr(toks, ctypes.c_int32), _ptr(par, ctypes.c_int32),
-                                   _ptr(temps, ctypes.c_float), B, N, V, D,
+                                   _ptr(temps, ctypes.c_float), B, N, V, D, int(sibling_rule),
                                    ctypes.c_uint64(seed), ctypes.c_uint64(offset),
                                    _ptr(rid, ctypes.c_int32), _ptr(out_t, ctypes.c_int32),
                                    _ptr(out_c, ctypes.c_int32), _ptr(out_p, ctypes.c_int32),
@@ -199,9 +209,9 @@ def verify_tree(target, draft, node_tokens, parent, temperature, max_depth, seed
     else:
         r = _c(uniforms[0], np.float64).reshape(B, N) if N > 0 else np.zeros((B, 1))
         u = _c(uniforms[1], np.float64).reshape(B, N + 1)
-        n = lib.oracle_verify_tree_u(target.ctypes.data, tdt, dptr, ddt, draft_kind,
+        n = lib.oracle_verify_tree_rule_u(target.ctypes.data, tdt, dptr, ddt, draft_kind,
                                      _ptr(toks, ctypes.c_int32), _ptr(par, ctypes.c_int32),
-                                     _ptr(temps, ctypes.c_float), B, N, V, D,
+                                     _ptr(temps, ctypes.c_float), B, N, V, D, int(sibling_rule),
                                      _ptr(r, ctypes.c_double), _ptr(u, ctypes.c_double),
                                      _ptr(out_t, ctypes.c_int32), _ptr(out_c, ctypes.c_int32),
                                      _ptr(out_p, ctypes.c_int32), _ptr(out_m, ctypes.c_double))

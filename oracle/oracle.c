@@ -316,12 +316,19 @@ int oracle_greedy_accept(const void *target, int tdt, const int32_t *tokens, int
  *  {-1} u [0, i).  r [B][N]: accept uniform of node i.  u [B][N+1]: draw uniform at
  *  row i.  Outputs: out_tokens [B][D+1], out_count [B], out_path [B][D] (accepted
  *  node indices), out_margin [B] (nullable).  Returns the number of invalid rows.
+ *  sibling_rule: ORC_SIBLINGS_WOR (0), siblings drafted without replacement: a
+ *  rejected token's draft probability is zeroed and q renormalised; ORC_SIBLINGS_IID
+ *  (1), siblings drafted i.i.d. from q: q is left as it is (the multi-draft rule of
+ *  SpecInfer-style verifiers; "Progressive Tree Drafting", section "검증", names the
+ *  without-replacement case).  Both keep p <- norm((p - q)+) after a rejection.
  */
-int oracle_verify_tree_u(const void *target, int tdt, const void *draft, int ddt, int dk,
-                         const int32_t *node_tokens, const int32_t *parent,
-                         const float *temperature, int B, int N, int V, int max_depth,
-                         const double *r, const double *u, int32_t *out_tokens,
-                         int32_t *out_count, int32_t *out_path, double *out_margin)
+#define ORC_SIBLINGS_WOR 0
+#define ORC_SIBLINGS_IID 1
+int oracle_verify_tree_rule_u(const void *target, int tdt, const void *draft, int ddt, int dk,
+                              const int32_t *node_tokens, const int32_t *parent,
+                              const float *temperature, int B, int N, int V, int max_depth,
+                              int sibling_rule, const double *r, const double *u, int32_t *out_tokens,
+                              int32_t *out_count, int32_t *out_path, double *out_margin)
 {
     double *w = (double *)malloc(sizeof(double) * (size_t)V);
     double *wn = (double *)malloc(sizeof(double) * (size_t)V);
@@ -383,7 +390,7 @@ int oracle_verify_tree_u(const void *target, int tdt, const void *draft, int ddt
                 double rc = r[(size_t)b * N + c];
                 margin = orc_min(margin, fabs(rc - ratio));
                 if (rc < ratio) { next = c; break; }
-                /* sibling rejected: p <- norm((p - q)+), q[x] <- 0, q <- norm(q) */
+                /* sibling rejected: p <- norm((p - q)+); without replacement also q[x] <- 0, q <- norm(q) */
                 double Zn = 0.0;
                 for (int i = 0; i < V; ++i) {
                     double d = w[i] / Zl - q[i];
@@ -394,6 +401,7 @@ int oracle_verify_tree_u(const void *target, int tdt, const void *draft, int ddt
                     memcpy(w, wn, sizeof(double) * (size_t)V);
                     Zl = Zn;
                 }
+                if (sibling_rule == ORC_SIBLINGS_IID) continue;
                 q[x] = 0.0;
                 double Sq = 0.0;
                 for (int i = 0; i < V; ++i) Sq += q[i];
@@ -428,13 +436,24 @@ int oracle_verify_tree_u(const void *target, int tdt, const void *draft, int ddt
     return n_invalid;
 }
 
+int oracle_verify_tree_u(const void *target, int tdt, const void *draft, int ddt, int dk,
+                         const int32_t *node_tokens, const int32_t *parent,
+                         const float *temperature, int B, int N, int V, int max_depth,
+                         const double *r, const double *u, int32_t *out_tokens,
+                         int32_t *out_count, int32_t *out_path, double *out_margin)
+{
+    return oracle_verify_tree_rule_u(target, tdt, draft, ddt, dk, node_tokens, parent, temperature, B, N, V,
+                                     max_depth, ORC_SIBLINGS_WOR, r, u, out_tokens, out_count, out_path,
+                                     out_margin);
+}
+
 /* Tree verify with the Philox stream (same slot layout as the chain, so a tree whose
  * parent array is a chain reproduces the chain's outputs). */
-int oracle_verify_tree(const void *target, int tdt, const void *draft, int ddt, int dk,
-                       const int32_t *node_tokens, const int32_t *parent, const float *temperature,
-                       int B, int N, int V, int max_depth, uint64_t seed, uint64_t offset,
-                       const int32_t *row_id, int32_t *out_tokens, int32_t *out_count,
-                       int32_t *out_path, double *out_margin)
+int oracle_verify_tree_rule(const void *target, int tdt, const void *draft, int ddt, int dk,
+                            const int32_t *node_tokens, const int32_t *parent, const float *temperature,
+                            int B, int N, int V, int max_depth, int sibling_rule, uint64_t seed,
+                            uint64_t offset, const int32_t *row_id, int32_t *out_tokens, int32_t *out_count,
+                            int32_t *out_path, double *out_margin)
 {
     double *r = (double *)malloc(sizeof(double) * (size_t)B * (N > 0 ? N : 1));
     double *u = (double *)malloc(sizeof(double) * (size_t)B * (N + 1));
@@ -447,11 +466,23 @@ int oracle_verify_tree(const void *target, int tdt, const void *draft, int ddt, 
             u[(size_t)b * (N + 1) + s] = uu;
         }
     }
-    int n = oracle_verify_tree_u(target, tdt, draft, ddt, dk, node_tokens, parent, temperature, B, N,
-                                 V, max_depth, r, u, out_tokens, out_count, out_path, out_margin);
+    int n = oracle_verify_tree_rule_u(target, tdt, draft, ddt, dk, node_tokens, parent, temperature, B, N,
+                                      V, max_depth, sibling_rule, r, u, out_tokens, out_count, out_path,
+                                      out_margin);
     free(r);
     free(u);
     return n;
+}
+
+int oracle_verify_tree(const void *target, int tdt, const void *draft, int ddt, int dk,
+                       const int32_t *node_tokens, const int32_t *parent, const float *temperature,
+                       int B, int N, int V, int max_depth, uint64_t seed, uint64_t offset,
+                       const int32_t *row_id, int32_t *out_tokens, int32_t *out_count,
+                       int32_t *out_path, double *out_margin)
+{
+    return oracle_verify_tree_rule(target, tdt, draft, ddt, dk, node_tokens, parent, temperature, B, N, V,
+                                   max_depth, ORC_SIBLINGS_WOR, seed, offset, row_id, out_tokens, out_count,
+                                   out_path, out_margin);
 }
 
 /* ------------------------------------------------------ tree attention mask */

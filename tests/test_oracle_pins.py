@@ -490,6 +490,76 @@ def test_tree_siblings_without_replacement_are_exact(V, T):
     np.testing.assert_allclose(law, p, atol=5e-6)
 
 
+def _root_two_children_law(t0, q32, T, pairs, weight, rule):
+    """Exact law of the first emitted token of a root with two children whose token
+    pairs come with the given weights, enumerating the oracle over the uniform grids."""
+    V = t0.size
+    n = len(pairs)
+    target = np.tile(np.stack([t0, t0, t0])[None], (n, 1, 1))
+    draft = np.tile(np.stack([q32, q32, q32])[None], (n, 1, 1))
+    toks = np.array(pairs, np.int32)
+    par = np.full((n, 2), -1, np.int32)
+
+    def run(idx, r1, r2, u0):
+        m = len(idx)
+        return oracle.verify_tree(target[idx], draft[idx], toks[idx], par[idx], np.full(m, T, np.float32), 1,
+                                  0, 0, draft_kind=oracle.DRAFT_PROBS, sibling_rule=rule,
+                                  uniforms=(np.stack([r1, r2], 1), np.stack([u0, u0, u0], 1)))
+
+    top = 1.0 - 1.0 / GRID
+    idx = np.arange(n)
+    p1 = _bisect_first_true(lambda k: run(idx, k / GRID, np.zeros(n), np.zeros(n))["path"][:, 0] != 0, n) / GRID
+    p2 = _bisect_first_true(lambda k: run(idx, np.full(n, top), k / GRID, np.zeros(n))["path"][:, 0] != 1,
+                            n) / GRID
+    rows = np.repeat(idx, V - 1)
+    thr = np.tile(np.arange(1, V), n)
+    m = len(rows)
+    bp = _bisect_first_true(lambda k: run(rows, np.full(m, top), np.full(m, top), k / GRID)["tokens"][:, 0] >= thr,
+                            m).reshape(n, V - 1)
+    law = np.zeros(V)
+    for j, (a, c) in enumerate(pairs):
+        res = np.diff(np.concatenate([[0], bp[j], [GRID]])) / GRID
+        law[a] += weight[j] * p1[j]
+        law[c] += weight[j] * (1 - p1[j]) * p2[j]
+        law += weight[j] * (1 - p1[j]) * (1 - p2[j]) * res
+    return law
+
+
+@pytest.mark.parametrize("V,T", [(5, 1.0), (4, 0.8)])
+def test_tree_siblings_iid_rule_is_exact_and_the_rules_differ(V, T):
+    """Multi-draft verification with children drawn i.i.d. from q (repeats allowed): the
+    i.i.d. rule (q left as it is after a rejection) gives law p_root exactly; the
+    without-replacement rule applied to the same drafts does not, and neither does the
+    i.i.d. rule applied to children drawn without replacement."""
+    rng = np.random.default_rng(V + 200)
+    t0 = rng.normal(0, 0.7, V).astype(np.float32)  # a flat p: the residual keeps several tokens
+    q32 = (rng.dirichlet(np.ones(V) * 2)).astype(np.float32)
+    q = q32.astype(np.float64) / q32.astype(np.float64).sum()
+    p = softmax64(t0.astype(np.float64) / np.float64(np.float32(T)))
+    iid_pairs = [(a, c) for a in range(V) for c in range(V)]
+    iid_w = np.array([q[a] * q[c] for a, c in iid_pairs])
+    law_iid = _root_two_children_law(t0, q32, T, iid_pairs, iid_w, oracle.SIBLINGS_IID)
+    np.testing.assert_allclose(law_iid, p, atol=5e-6)
+    law_mixed = _root_two_children_law(t0, q32, T, iid_pairs, iid_w, oracle.SIBLINGS_WOR)
+    assert np.abs(law_mixed - p).max() > 1e-3
+    wor_pairs = [(a, c) for a in range(V) for c in range(V) if a != c]
+    wor_w = np.array([q[a] * q[c] / (1 - q[a]) for a, c in wor_pairs])
+    law_wor = _root_two_children_law(t0, q32, T, wor_pairs, wor_w, oracle.SIBLINGS_WOR)
+    np.testing.assert_allclose(law_wor, p, atol=5e-6)
+    assert np.abs(_root_two_children_law(t0, q32, T, wor_pairs, wor_w, oracle.SIBLINGS_IID) - p).max() > 1e-3
+
+
+def test_sibling_rules_agree_for_a_single_child_and_on_chains():
+    """The two rules differ only after a rejection among siblings: with at most one
+    child per node (a chain) they give identical results."""
+    w = synth.chain_as_tree(synth.tiny_chain(seed=8, V=64, K=4, B=40))
+    args = (w["target"], w["draft"], w["node_tokens"], w["parent"], w["temperature"], w["max_depth"], 3, 1)
+    a = oracle.verify_tree(*args, draft_kind=w["draft_kind"], sibling_rule=oracle.SIBLINGS_WOR)
+    b = oracle.verify_tree(*args, draft_kind=w["draft_kind"], sibling_rule=oracle.SIBLINGS_IID)
+    for k in ("tokens", "count", "path", "margin"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
 # ------------------------------------------------------------ bad inputs
 
 def test_invalid_rows_give_count_zero():
