@@ -67,12 +67,14 @@ def _load():
                                                   f64p, f64p, i32p, i32p, i32p, f64p]
         lib.oracle_verify_tree_rule.argtypes = [vp, ci, vp, ci, ci, i32p, i32p, f32p, ci, ci, ci, ci, ci,
                                                 u64, u64, i32p, i32p, i32p, i32p, f64p]
+        lib.oracle_sample_and_verify.argtypes = [vp, ci, vp, ci, f32p, ci, ci, ci, u64, u64, i32p, i32p, i32p,
+                                                 i32p, f32p, f64p]
         lib.oracle_tree_mask.argtypes = [i32p, ci, ci, vp, i32p, i32p]
         lib.oracle_kv_compact.argtypes = [vp, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t, i32p, i32p, i32p,
                                           ci, ci, ci]
         for name in ("oracle_verify_chain_u", "oracle_verify_chain", "oracle_greedy_accept",
                      "oracle_verify_tree_u", "oracle_verify_tree", "oracle_tree_mask", "oracle_kv_compact",
-                     "oracle_verify_tree_rule_u", "oracle_verify_tree_rule"):
+                     "oracle_verify_tree_rule_u", "oracle_verify_tree_rule", "oracle_sample_and_verify"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -216,6 +218,35 @@ def verify_tree(target, draft, node_tokens, parent, temperature, max_depth, seed
                                      _ptr(out_t, ctypes.c_int32), _ptr(out_c, ctypes.c_int32),
                                      _ptr(out_p, ctypes.c_int32), _ptr(out_m, ctypes.c_double))
     return dict(tokens=out_t, count=out_c, path=out_p[:, :D], margin=out_m, n_invalid=n)
+
+
+def sample_and_verify(target, draft, temperature, seed, offset, row_id=None):
+    """Draft sampling and verify in one step: x_k ~ softmax(draft_k / T) by the Philox
+    word-2 uniform of slot k (argmax for greedy rows), then the chain verify of x.
+    target [B][K+1][V], draft logits [B][K][V].  Returns dict(draft_tokens, tokens,
+    count, accept_prob, margin, n_invalid)."""
+    lib = _load()
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    B, K1, V = target.shape
+    K = K1 - 1
+    if draft.shape != (B, K, V):
+        raise ValueError(f"draft shape {draft.shape} != {(B, K, V)}")
+    temps = _c(temperature, np.float32).reshape(B)
+    rid = None if row_id is None else _c(row_id, np.int32)
+    xd = np.full((B, max(K, 1)), -1, np.int32)
+    out_t = np.full((B, K + 1), -1, np.int32)
+    out_c = np.zeros(B, np.int32)
+    out_ap = np.full((B, max(K, 1)), -1, np.float32)
+    out_m = np.zeros(B, np.float64)
+    n = lib.oracle_sample_and_verify(target.ctypes.data, _logits_dtype(target), draft.ctypes.data,
+                                     _logits_dtype(draft), _ptr(temps, ctypes.c_float), B, K, V,
+                                     ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(rid, ctypes.c_int32),
+                                     _ptr(xd, ctypes.c_int32), _ptr(out_t, ctypes.c_int32),
+                                     _ptr(out_c, ctypes.c_int32), _ptr(out_ap, ctypes.c_float),
+                                     _ptr(out_m, ctypes.c_double))
+    return dict(draft_tokens=xd[:, :K], tokens=out_t, count=out_c, accept_prob=out_ap[:, :K], margin=out_m,
+                n_invalid=n)
 
 
 def tree_mask(parent):

@@ -559,3 +559,63 @@ int oracle_kv_compact(unsigned char *kv, size_t batch_stride, size_t row_stride,
     }
     return skipped;
 }
+
+/* ------------------------------------------------- draft sampling + verify */
+
+/*
+ * The draft side of a round done in the same call as the verify: each drafted token
+ * x_k is drawn from q_k = softmax(draft_logits_k / T) ("[논문 리뷰] Fast Inference
+ * from Transformers via Speculative Decoding", section 2, Step 1: the draft model
+ * proposes x_1..x_K by sampling; "Speculative Decoding and EAGLE", section "개념"),
+ * then the K tokens are verified exactly as oracle_verify_chain does with the
+ * drafts given as logits.  The draft uniform of position k is word 2 of Philox slot
+ * k (words 0 and 1 stay the accept and draw uniforms), on the same 24-bit grid; the
+ * token is the inverse-CDF draw of that uniform from q_k.  Greedy rows (T <= 0)
+ * draft x_k = argmax of draft row k (lowest index on ties) and verify greedily.
+ *  target [B][K+1][V], draft [B][K][V] logits; out_draft_tokens [B][K] (-1 for a
+ *  draft row that is invalid data, which makes the whole batch row invalid);
+ *  other outputs as oracle_verify_chain.  out_margin also covers the draft draws.
+ */
+int oracle_sample_and_verify(const void *target, int tdt, const void *draft, int ddt,
+                             const float *temperature, int B, int K, int V, uint64_t seed,
+                             uint64_t offset, const int32_t *row_id, int32_t *out_draft_tokens,
+                             int32_t *out_tokens, int32_t *out_count, float *out_accept_prob,
+                             double *out_margin)
+{
+    double *q = (double *)malloc(sizeof(double) * (size_t)V);
+    int n_invalid = 0;
+    for (int b = 0; b < B; ++b) {
+        const uint64_t rid = row_id ? (uint64_t)row_id[b] : (uint64_t)b;
+        const double T = (double)temperature[b];
+        const int greedy = !(T > 0.0);
+        int32_t *xd = out_draft_tokens + (size_t)b * K;
+        double margin = INFINITY;
+        for (int k = 0; k < K; ++k) {
+            const size_t off = ((size_t)b * K + k) * (size_t)V;
+            if (greedy) {
+                double m;
+                int g;
+                xd[k] = orc_row_max(draft, ddt, off, V, &m, &g) ? -1 : g;
+                continue;
+            }
+            if (orc_softmax(draft, ddt, off, V, T, q)) { xd[k] = -1; continue; }
+            uint64_t c[4] = {(uint64_t)k, rid, offset, 0}, key[2] = {seed, 0}, w[4];
+            oracle_philox4x64_10(c, key, w);
+            double mg;
+            xd[k] = orc_draw(q, V, orc_u24(w[2]), &mg);
+            margin = orc_min(margin, mg);
+        }
+        const size_t tro = (size_t)b * (K + 1) * (size_t)V, dro = (size_t)b * K * (size_t)V;
+        const size_t tsz = tdt == ORC_F32 ? 4 : 2, dsz = ddt == ORC_F32 ? 4 : 2;
+        double vm = INFINITY;
+        const int32_t rid32 = (int32_t)rid;
+        n_invalid += oracle_verify_chain((const char *)target + tro * tsz, tdt, (const char *)draft + dro * dsz,
+                                         ddt, ORC_DRAFT_LOGITS, xd, temperature + b, 1, K, V, seed, offset,
+                                         &rid32, out_tokens + (size_t)b * (K + 1), out_count + b,
+                                         out_accept_prob ? out_accept_prob + (size_t)b * (K > 0 ? K : 1) : NULL,
+                                         &vm);
+        if (out_margin) out_margin[b] = orc_min(margin, vm);
+    }
+    free(q);
+    return n_invalid;
+}
