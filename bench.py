@@ -10,7 +10,7 @@ through them; steps are replayed from CUDA graphs so that host launch gaps do
 not enter the device timing.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--workload single_stream|large_batch|mixed_batch|tree|tree_mask|kv_compact]
+                  [--workload single_stream|large_batch|mixed_batch|sample_verify|tree|tree_iid|tree_mask|kv_compact]
 
 tree_mask and kv_compact time the steps on either side of a tree verify (the
 ancestor attention mask of each draft tree; moving the accepted branch's KV-cache
@@ -67,9 +67,19 @@ def make_workload(name: str, rank: int, rounds: int, batch: int = 0, temperature
     if name == "mixed_batch":
         w = synth.mixed_batch(seed=seed)
         return dict(w, per_step_rows=64, desc="mixed greedy/sampling chain verify B=64 K=5 V=32000, bf16 logits")
+    if name == "sample_verify":
+        w = synth.mixed_batch(seed=seed)
+        return dict(w, per_step_rows=64, sample=True,
+                    desc="draft sampling + chain verify in one call, B=64 K=5 V=32000, bf16 logits, "
+                         "greedy/sampling rows mixed")
     if name == "tree":
         w = synth.tree(seed=seed, temperature=1.0)
         return dict(w, per_step_rows=16, desc="tree verify B=16 N=60 depth<=6 V=128256 T=1, bf16 logits")
+    if name == "tree_iid":
+        w = synth.redraw_children_iid(synth.tree(seed=seed, temperature=1.0), seed=seed)
+        return dict(w, per_step_rows=16, sibling_rule="iid",
+                    desc="multi-draft tree verify B=16 N=60 depth<=6 V=128256 T=1, children drawn i.i.d. from q "
+                         "(i.i.d. sibling rule), bf16 logits")
     raise ValueError(name)
 
 
@@ -233,6 +243,8 @@ def run_ours(args, rank, world, device):
     sv.lib()
     w = make_workload(args.workload, rank, args.rounds, args.batch, args.temperature)
     tree = w["kind"] == "tree"
+    rule = w.get("sibling_rule", "without_replacement")
+    sample = bool(w.get("sample"))
     per_step_rows = w["per_step_rows"]
     stream = torch.cuda.Stream(device)
     torch.cuda.set_stream(stream)
@@ -257,13 +269,18 @@ def run_ours(args, rank, world, device):
     else:
         out_t = torch.empty((chunk, per_step_rows, K_ + 1), dtype=torch.int32, device=device)
         out_c = torch.empty((chunk, per_step_rows), dtype=torch.int32, device=device)
+        out_x = torch.empty((chunk, per_step_rows, K_), dtype=torch.int32, device=device)
 
     def step(i, slot):
         r = (i % n_inputs) * per_step_rows
         sl = slice(r, r + per_step_rows)
         if tree:
             sv.spec_verify_tree(dt[sl], dd[sl], dtok[sl], dpar[sl], dtemp[sl], D, 17, i, draft_kind=kind,
-                                out_tokens=out_t[slot], out_count=out_c[slot], out_path=out_p[slot])
+                                out_tokens=out_t[slot], out_count=out_c[slot], out_path=out_p[slot],
+                                sibling_rule=rule)
+        elif sample:
+            sv.spec_sample_and_verify(dt[sl], dd[sl], dtemp[sl], 17, i, out_draft_tokens=out_x[slot],
+                                      out_tokens=out_t[slot], out_count=out_c[slot])
         else:
             sv.spec_verify_chain(dt[sl], dd[sl], dtok[sl], dtemp[sl], 17, i, draft_kind=kind,
                                  out_tokens=out_t[slot], out_count=out_c[slot])
@@ -319,7 +336,10 @@ def run_ours(args, rank, world, device):
         bytes_steps = []
         for s in range(steps_in_chunk):
             r = (s % n_inputs) * per_step_rows
-            bytes_steps.append(algorithmic_bytes_chain(w, range(r, r + per_step_rows), counts[s]))
+            b = algorithmic_bytes_chain(w, range(r, r + per_step_rows), counts[s])
+            if sample:  # every draft row is read once more to draw the proposals
+                b += per_step_rows * K_ * w["draft"].shape[2] * w["draft"].dtype.itemsize
+            bytes_steps.append(b)
     bytes_per_launch = float(np.mean(bytes_steps))
     mean_count = float(counts.mean())
 
@@ -403,7 +423,10 @@ def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
         dtemp.copy_(htemp, non_blocking=True)
         if tree:
             dpar.copy_(hpar, non_blocking=True)
-            ot, oc, _ = sv.spec_verify_tree(dt, dd, dtok, dpar, dtemp, D, 23, i, draft_kind=kind)
+            ot, oc, _ = sv.spec_verify_tree(dt, dd, dtok, dpar, dtemp, D, 23, i, draft_kind=kind,
+                                            sibling_rule=w.get("sibling_rule", "without_replacement"))
+        elif w.get("sample"):
+            _, ot, oc, _ = sv.spec_sample_and_verify(dt, dd, dtemp, 23, i)
         else:
             ot, oc, _ = sv.spec_verify_chain(dt, dd, dtok, dtemp, 23, i, draft_kind=kind)
         ho_t.copy_(ot, non_blocking=True)
@@ -435,10 +458,14 @@ def run_cpu_baseline(w, per_step_rows, n_inputs, tree, budget_s=10.0):
         sl = slice(r, r + per_step_rows)
         if tree:
             oracle.verify_tree(w["target"][sl], w["draft"][sl], w["node_tokens"][sl], w["parent"][sl],
-                               w["temperature"][sl], w["max_depth"], 17, i, draft_kind=w["draft_kind"])
+                               w["temperature"][sl], w["max_depth"], 17, i, draft_kind=w["draft_kind"],
+                               sibling_rule=1 if w.get("sibling_rule") == "iid" else 0)
         else:
-            oracle.verify_chain(w["target"][sl], w["draft"][sl], w["tokens"][sl], w["temperature"][sl], 17, i,
-                                draft_kind=w["draft_kind"])
+            if w.get("sample"):
+                oracle.sample_and_verify(w["target"][sl], w["draft"][sl], w["temperature"][sl], 17, i)
+            else:
+                oracle.verify_chain(w["target"][sl], w["draft"][sl], w["tokens"][sl], w["temperature"][sl], 17, i,
+                                    draft_kind=w["draft_kind"])
         done += per_step_rows
         i += 1
     el = time.perf_counter() - t0
@@ -465,10 +492,14 @@ def run_reference(args, rank):
         sl = slice(r, r + per_step_rows)
         if tree:
             oracle.verify_tree(w["target"][sl], w["draft"][sl], w["node_tokens"][sl], w["parent"][sl],
-                               w["temperature"][sl], w["max_depth"], 17, i, draft_kind=w["draft_kind"])
+                               w["temperature"][sl], w["max_depth"], 17, i, draft_kind=w["draft_kind"],
+                               sibling_rule=1 if w.get("sibling_rule") == "iid" else 0)
         else:
-            oracle.verify_chain(w["target"][sl], w["draft"][sl], w["tokens"][sl], w["temperature"][sl], 17, i,
-                                draft_kind=w["draft_kind"])
+            if w.get("sample"):
+                oracle.sample_and_verify(w["target"][sl], w["draft"][sl], w["temperature"][sl], 17, i)
+            else:
+                oracle.verify_chain(w["target"][sl], w["draft"][sl], w["tokens"][sl], w["temperature"][sl], 17, i,
+                                    draft_kind=w["draft_kind"])
 
     for i in range(max(args.warmup, 3)):
         one(i)
@@ -751,7 +782,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="single_stream",
-                    choices=["single_stream", "large_batch", "mixed_batch", "tree", "tree_mask", "kv_compact"])
+                    choices=["single_stream", "large_batch", "mixed_batch", "sample_verify", "tree", "tree_iid",
+                             "tree_mask", "kv_compact"])
     ap.add_argument("--rounds", type=int, default=64, help="resident rounds of the single-stream workload")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--batch", type=int, default=0,

@@ -185,6 +185,54 @@ SV_API sv_status spec_verify_tree(const void *target_logits, sv_dtype tdt,
                            int32_t *out_tokens, int32_t *out_count, int32_t *out_path,
                            void *stream);
 
+/*
+ * Draft sampling and verify in one call, for drafters whose K next-token
+ * distributions are all known up front (several prediction heads on one hidden
+ * state): x_k is drawn from q_k = softmax(draft_logits_k / T) ("[논문 리뷰] Fast
+ * Inference from Transformers via Speculative Decoding", section 2, Step 1: the
+ * draft proposes by sampling from its own distribution), then the K tokens are
+ * verified exactly as spec_verify_chain does with the draft given as logits.
+ *   draft_logits   device [B][K][V] (ddt); the same array q is computed from in the verify.
+ *   out_draft_tokens device int32 [B][K]: the drafted tokens (-1 where a draft row is
+ *                  invalid data, which makes that batch row invalid: count 0).
+ * x_k is the inverse-CDF draw of word 2 of Philox slot k (words 0 and 1 keep their
+ * roles), on the same 24-bit grid; a greedy row (T <= 0) drafts x_k = argmax of
+ * draft row k (lowest index on ties) and is verified greedily.  Other arguments,
+ * outputs, workspace use and errors as spec_verify_chain.  Two kernels run on
+ * `stream`: the sampling kernel, then the verify kernel.
+ */
+SV_API sv_status spec_sample_and_verify(const void *target_logits, sv_dtype tdt,
+                                        const void *draft_logits, sv_dtype ddt,
+                                        const float *temperature, int B, int K, int V,
+                                        uint64_t seed, uint64_t offset, int32_t *out_draft_tokens,
+                                        int32_t *out_tokens, int32_t *out_count, float *out_accept_prob,
+                                        void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * How the children of one node were drafted, which decides what a rejection does
+ * to the draft distribution before the next sibling is tried ("Progressive Tree
+ * Drafting" summary, section "검증": sampling acceptance without replacement;
+ * drafts sampled independently from q are the multi-draft case of the same rule).
+ *  SV_SIBLINGS_WITHOUT_REPLACEMENT: the children are distinct tokens drawn without
+ *    replacement from q; after rejecting token x, q(x) <- 0 and q is renormalised.
+ *  SV_SIBLINGS_IID: the children were drawn independently from q (a token may
+ *    repeat); q is left as it is.
+ * Both set p <- (p - q)+ / |(p - q)+|_1 after a rejection, and both give outputs
+ * distributed exactly as the target when the children were drafted that way.
+ */
+typedef enum { SV_SIBLINGS_WITHOUT_REPLACEMENT = 0, SV_SIBLINGS_IID = 1 } sv_sibling_rule;
+
+/* spec_verify_tree with an explicit sibling rule (spec_verify_tree uses
+ * SV_SIBLINGS_WITHOUT_REPLACEMENT).  Same arguments, outputs and errors, plus
+ * SV_ERR_INVALID_ARG for an unknown rule. */
+SV_API sv_status spec_verify_tree_rule(const void *target_logits, sv_dtype tdt,
+                                       const void *draft, sv_dtype ddt, sv_draft_kind dk,
+                                       const int32_t *node_tokens, const int32_t *parent,
+                                       const float *temperature, int B, int N, int V, int max_depth,
+                                       sv_sibling_rule sibling_rule, uint64_t seed, uint64_t offset,
+                                       int32_t *out_tokens, int32_t *out_count, int32_t *out_path,
+                                       void *stream);
+
 /* Static, NUL-terminated description of a status code. */
 SV_API const char *spec_verify_status_string(sv_status status);
 

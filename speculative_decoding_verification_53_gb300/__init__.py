@@ -21,10 +21,11 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_TIMEOUT, SV_ERR_BAD_INPUT = range(6)
 SV_F32, SV_BF16 = 0, 1
 SV_DRAFT_PROBS, SV_DRAFT_LOGITS = 0, 1
+SV_SIBLINGS_WITHOUT_REPLACEMENT, SV_SIBLINGS_IID = 0, 1
 
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_chain", "spec_greedy_accept", "spec_verify_tree",
            "spec_verify_status_string", "spec_verify_last_cuda_error", "spec_verify_chain_noalloc",
-           "spec_tree_mask", "spec_kv_compact")
+           "spec_tree_mask", "spec_kv_compact", "spec_verify_tree_rule", "spec_sample_and_verify")
 
 _lib = None
 
@@ -58,6 +59,11 @@ def lib() -> ctypes.CDLL:
     L.spec_greedy_accept.restype = ci
     L.spec_verify_tree.argtypes = [vp, ci, vp, ci, ci, vp, vp, vp, ci, ci, ci, ci, u64, u64, vp, vp, vp, vp]
     L.spec_verify_tree.restype = ci
+    L.spec_verify_tree_rule.argtypes = [vp, ci, vp, ci, ci, vp, vp, vp, ci, ci, ci, ci, ci, u64, u64, vp, vp, vp,
+                                        vp]
+    L.spec_verify_tree_rule.restype = ci
+    L.spec_sample_and_verify.argtypes = [vp, ci, vp, ci, vp, ci, ci, ci, u64, u64, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_sample_and_verify.restype = ci
     L.spec_tree_mask.argtypes = [vp, ci, ci, vp, vp, vp, vp]
     L.spec_tree_mask.restype = ci
     i64 = ctypes.c_int64
@@ -215,6 +221,42 @@ def spec_verify_chain_noalloc(target_logits, draft, draft_tokens, temperature, s
     return out_tokens, out_count, out_accept_prob
 
 
+def spec_sample_and_verify(target_logits, draft_logits, temperature, seed: int, offset: int, *,
+                           out_draft_tokens=None, out_tokens=None, out_count=None, out_accept_prob=None,
+                           want_accept_prob: bool = False, workspace="auto", stream=None):
+    """Draft sampling and verify in one call: x_k ~ softmax(draft_logits_k / T) (argmax for
+    greedy rows), then the chain verify of those tokens.  target_logits [B][K+1][V],
+    draft_logits [B][K][V], temperature fp32 [B].  Returns (out_draft_tokens [B][K],
+    out_tokens [B][K+1], out_count [B], out_accept_prob [B][K] or None)."""
+    torch = _torch()
+    _dev(target_logits, "target_logits")
+    _dev(draft_logits, "draft_logits")
+    _dev(temperature, "temperature", torch.float32)
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    if tuple(draft_logits.shape) != (B, K, V):
+        raise ValueError(f"draft_logits shape {tuple(draft_logits.shape)} != {(B, K, V)}")
+    dev = target_logits.device
+    if out_draft_tokens is None:
+        out_draft_tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_count is None:
+        out_count = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_accept_prob is None and want_accept_prob:
+        out_accept_prob = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if isinstance(workspace, str):
+        workspace = _auto_workspace(B, K, V, stream) if B > 0 else None
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    st = lib().spec_sample_and_verify(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft_logits),
+                                      _dtype_code(draft_logits), _ptr(temperature), B, K, V, int(seed), int(offset),
+                                      _ptr(out_draft_tokens), _ptr(out_tokens), _ptr(out_count),
+                                      _ptr(out_accept_prob), ws_ptr, ws_bytes, _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_sample_and_verify")
+    return out_draft_tokens, out_tokens, out_count, out_accept_prob
+
+
 def spec_greedy_accept(target_logits, draft_tokens, *, out_tokens=None, out_count=None, stream=None):
     """Greedy acceptance for every row.  Returns (out_tokens [B][K+1], out_count [B])."""
     torch = _torch()
@@ -235,9 +277,12 @@ def spec_greedy_accept(target_logits, draft_tokens, *, out_tokens=None, out_coun
 
 
 def spec_verify_tree(target_logits, draft, node_tokens, parent, temperature, max_depth: int, seed: int,
-                     offset: int, *, draft_kind, out_tokens=None, out_count=None, out_path=None, stream=None):
+                     offset: int, *, draft_kind, out_tokens=None, out_count=None, out_path=None,
+                     sibling_rule="without_replacement", stream=None):
     """Tree verify.  target_logits/draft [B][N+1][V], node_tokens/parent int32 [B][N],
-    temperature fp32 [B].  Returns (out_tokens [B][D+1], out_count [B], out_path [B][D])."""
+    temperature fp32 [B].  sibling_rule: "without_replacement" (children drawn without
+    replacement from q) or "iid" (drawn independently; a token may repeat).
+    Returns (out_tokens [B][D+1], out_count [B], out_path [B][D])."""
     torch = _torch()
     _dev(target_logits, "target_logits")
     B, N1, V = target_logits.shape
@@ -257,9 +302,13 @@ def spec_verify_tree(target_logits, draft, node_tokens, parent, temperature, max
         out_count = torch.empty((B,), dtype=torch.int32, device=dev)
     if out_path is None:
         out_path = torch.empty((B, D), dtype=torch.int32, device=dev)
-    st = lib().spec_verify_tree(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), _dtype_code(draft),
-                                dk, _ptr(node_tokens), _ptr(parent), _ptr(temperature), B, N, V, D, int(seed),
-                                int(offset), _ptr(out_tokens), _ptr(out_count), _ptr(out_path), _stream(stream))
+    rules = {"without_replacement": SV_SIBLINGS_WITHOUT_REPLACEMENT, "iid": SV_SIBLINGS_IID}
+    if sibling_rule not in rules:
+        raise ValueError("sibling_rule must be 'without_replacement' or 'iid'")
+    st = lib().spec_verify_tree_rule(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft),
+                                     _dtype_code(draft), dk, _ptr(node_tokens), _ptr(parent), _ptr(temperature), B,
+                                     N, V, D, rules[sibling_rule], int(seed), int(offset), _ptr(out_tokens),
+                                     _ptr(out_count), _ptr(out_path), _stream(stream))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_tree")
     return out_tokens, out_count, out_path

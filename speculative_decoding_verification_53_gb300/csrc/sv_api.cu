@@ -236,6 +236,29 @@ sv_status spec_verify_chain(const void* target_logits, sv_dtype tdt, const void*
     return run_chain(a, tdt, ddt, dk, K > 0, info.sms, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
+sv_status spec_sample_and_verify(const void* target_logits, sv_dtype tdt, const void* draft_logits, sv_dtype ddt,
+                                 const float* temperature, int B, int K, int V, uint64_t seed, uint64_t offset,
+                                 int32_t* out_draft_tokens, int32_t* out_tokens, int32_t* out_count,
+                                 float* out_accept_prob, void* workspace, size_t ws_bytes, void* stream) {
+    if (B < 0 || B > kMaxB || K < 0 || K > kMaxK || V < 1 || V > kMaxV) return SV_ERR_INVALID_ARG;
+    if (!is_dtype(tdt) || !is_dtype(ddt)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !temperature || !out_tokens || !out_count || (K > 0 && (!draft_logits || !out_draft_tokens)))
+        return SV_ERR_INVALID_ARG;
+    DeviceInfo info;
+    sv_status st = device_info(info);
+    if (st != SV_OK) return st;
+    if (K > 0) {
+        const sv::SampleArgs s{draft_logits, temperature, B, K, V, seed, offset, out_draft_tokens};
+        const cudaError_t e = sv::launch_draft_sample(s, ddt, info.sms, (cudaStream_t)stream);
+        if (e != cudaSuccess) return launch_status(e);
+    }
+    // the verify reads the tokens the sampling kernel wrote (same stream, so in order)
+    const sv::ChainArgs a{target_logits, draft_logits, out_draft_tokens, temperature, B, K, V, seed, offset,
+                          out_tokens, out_count, out_accept_prob};
+    return run_chain(a, tdt, ddt, SV_DRAFT_LOGITS, K > 0, info.sms, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
 sv_status spec_greedy_accept(const void* target_logits, sv_dtype tdt, const int32_t* draft_tokens, int B, int K,
                              int V, int32_t* out_tokens, int32_t* out_count, void* stream) {
     if (B < 0 || B > kMaxB || K < 0 || K > kMaxK || V < 1 || V > kMaxV) return SV_ERR_INVALID_ARG;
@@ -255,8 +278,20 @@ sv_status spec_verify_tree(const void* target_logits, sv_dtype tdt, const void* 
                            const float* temperature, int B, int N, int V, int max_depth, uint64_t seed,
                            uint64_t offset, int32_t* out_tokens, int32_t* out_count, int32_t* out_path,
                            void* stream) {
+    return spec_verify_tree_rule(target_logits, tdt, draft, ddt, dk, node_tokens, parent, temperature, B, N, V,
+                                 max_depth, SV_SIBLINGS_WITHOUT_REPLACEMENT, seed, offset, out_tokens, out_count,
+                                 out_path, stream);
+}
+
+sv_status spec_verify_tree_rule(const void* target_logits, sv_dtype tdt, const void* draft, sv_dtype ddt,
+                                sv_draft_kind dk, const int32_t* node_tokens, const int32_t* parent,
+                                const float* temperature, int B, int N, int V, int max_depth,
+                                sv_sibling_rule sibling_rule, uint64_t seed, uint64_t offset, int32_t* out_tokens,
+                                int32_t* out_count, int32_t* out_path, void* stream) {
     if (B < 0 || B > kMaxB || N < 1 || N > kMaxNodes || V < 1 || V > kMaxV || max_depth < 1 ||
         max_depth > kMaxDepth)
+        return SV_ERR_INVALID_ARG;
+    if (sibling_rule != SV_SIBLINGS_WITHOUT_REPLACEMENT && sibling_rule != SV_SIBLINGS_IID)
         return SV_ERR_INVALID_ARG;
     if (!is_dtype(tdt) || !is_dtype(ddt)) return SV_ERR_INVALID_ARG;
     if (dk != SV_DRAFT_PROBS && dk != SV_DRAFT_LOGITS) return SV_ERR_INVALID_ARG;
@@ -269,7 +304,7 @@ sv_status spec_verify_tree(const void* target_logits, sv_dtype tdt, const void* 
     sv_status st = device_info(info);
     if (st != SV_OK) return st;
     sv::TreeArgs a{target_logits, draft, node_tokens, parent, temperature, B, N, V, max_depth, seed, offset,
-                   out_tokens, out_count, out_path};
+                   out_tokens, out_count, out_path, (int)sibling_rule};
     const int G = sv::choose_cluster(B, V, info.sms);
     // shared-memory staged walk (with the children's rows prefetched) when rows are aligned
     const size_t tsz = dtype_size(tdt), dsz = dk == SV_DRAFT_PROBS ? 4 : dtype_size(ddt);

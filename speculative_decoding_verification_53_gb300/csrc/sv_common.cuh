@@ -80,6 +80,13 @@ __device__ __forceinline__ void slot_uniforms(uint64_t seed, uint64_t offset, ui
     u = (float)(uint32_t)(x1 >> 40) * (1.0f / 16777216.0f);
 }
 
+// The draft-sampling uniform of a Philox slot: word 2, on the same 24-bit grid.
+__device__ __forceinline__ float slot_draft_uniform(uint64_t seed, uint64_t offset, uint64_t row, uint64_t slot) {
+    uint64_t x0 = slot, x1 = row, x2 = offset, x3 = 0;
+    philox4x64_10(x0, x1, x2, x3, seed, 0);
+    return (float)(uint32_t)(x2 >> 40) * (1.0f / 16777216.0f);
+}
+
 // ----------------------------------------------------------------- loads
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {

@@ -37,6 +37,15 @@ struct TreeArgs {
     int32_t* out_tokens;       // [B][D+1]
     int32_t* out_count;        // [B]
     int32_t* out_path;         // [B][D]
+    int sibling_rule;          // SV_SIBLINGS_WITHOUT_REPLACEMENT or SV_SIBLINGS_IID
+};
+
+struct SampleArgs {
+    const void* draft;         // [B][K][V] draft logits
+    const float* temperature;  // [B]
+    int B, K, V;
+    uint64_t seed, offset;
+    int32_t* out_draft_tokens; // [B][K]
 };
 
 // Shared-memory layout of the staged chain kernel (host-computed per launch).
@@ -81,5 +90,8 @@ cudaError_t launch_tree(const TreeArgs& a, int tdt, int ddt, int dk, int cluster
 
 // Dynamic shared memory (tile sums of the draw) for a row split `cluster` ways.
 size_t draw_smem_bytes(int V, int cluster);
+
+// Draft tokens x_k ~ softmax(draft_k / T) (argmax for greedy rows) for every (b, k).
+cudaError_t launch_draft_sample(const SampleArgs& a, int ddt, int num_sms, cudaStream_t stream);
 
 }  // namespace sv

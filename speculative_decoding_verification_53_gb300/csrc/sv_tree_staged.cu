@@ -270,10 +270,13 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
                 }
                 const float2 tot = cluster_sum2(part, sc, phase);
                 if (threadIdx.x == 0) {
-                    hs.x[nh] = x;
+                    // without replacement the tried token leaves q and q is renormalised;
+                    // i.i.d. siblings leave q as it is (no token recorded, no rescale)
+                    const bool iid = a.sibling_rule == SV_SIBLINGS_IID;
+                    hs.x[nh] = iid ? -1 : x;
                     hs.applied[nh] = tot.x > 0.f ? 1 : 0;
                     hs.zinv[nh + 1] = tot.x > 0.f ? 1.f / tot.x : hs.zinv[nh];
-                    hs.qs[nh + 1] = tot.y > 0.f ? hs.qs[nh] / tot.y : hs.qs[nh];
+                    hs.qs[nh + 1] = (!iid && tot.y > 0.f) ? hs.qs[nh] / tot.y : hs.qs[nh];
                     hs.n = nh + 1;
                 }
                 __syncthreads();

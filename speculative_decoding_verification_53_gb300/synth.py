@@ -342,3 +342,33 @@ def kv_cache(seed: int, n_buffers: int, B: int, planes: int, rows: int, row_byte
     layer and K/V; a plane is a KV head; a row is one token's head vector)."""
     rng = np.random.default_rng([seed, 13])
     return rng.integers(0, 256, (n_buffers, B, planes, rows, row_bytes), dtype=np.uint8)
+
+
+def redraw_children_iid(w: dict, seed: int) -> dict:
+    """The tree of ``w`` with every node's token redrawn independently from its parent's
+    draft distribution (the row the node was proposed from), so siblings may repeat:
+    the drafts of a multi-draft verifier that samples each child i.i.d. from q.
+    Draft logits are turned into q with the row's temperature (1 for greedy rows)."""
+    out = dict(w)
+    toks = w["node_tokens"].copy()
+    B, N = toks.shape
+    for b in range(B):
+        rng = np.random.default_rng([seed, b, 17])
+        T = float(w["temperature"][b]) if w["temperature"][b] > 0 else 1.0
+        cache = {}
+        for i in range(N):
+            row = int(w["parent"][b, i]) + 1
+            if row not in cache:
+                d = w["draft"][b, row]
+                d = bf16_bits_to_f32(d) if d.dtype == np.uint16 else d.astype(np.float32)
+                if w["draft_kind"] == 0:
+                    q = d.astype(np.float64)
+                else:
+                    z = d.astype(np.float64) / T
+                    q = np.exp(z - z.max())
+                q = q / q.sum()
+                cache[row] = np.cumsum(q)
+            cdf = cache[row]
+            toks[b, i] = min(int(np.searchsorted(cdf, rng.random() * cdf[-1], side="right")), cdf.size - 1)
+    out["node_tokens"] = toks
+    return out

@@ -54,7 +54,10 @@ def oracle_chain(w, seed=None, offset=None, rows=None):
                                draft_kind=w["draft_kind"], row_id=rows.astype(np.int32))
 
 
-def gpu_tree(w, seed=None, offset=None):
+RULE_NAMES = {oracle.SIBLINGS_WOR: "without_replacement", oracle.SIBLINGS_IID: "iid"}
+
+
+def gpu_tree(w, seed=None, offset=None, sibling_rule=oracle.SIBLINGS_WOR):
     import torch
     import speculative_decoding_verification_53_gb300 as sv
     seed = w["seed"] if seed is None else seed
@@ -62,19 +65,19 @@ def gpu_tree(w, seed=None, offset=None):
     ot, oc, op = sv.spec_verify_tree(to_dev(w["target"]), to_dev(w["draft"]),
                                      to_dev(w["node_tokens"].astype(np.int32)), to_dev(w["parent"].astype(np.int32)),
                                      to_dev(w["temperature"].astype(np.float32)), w["max_depth"], seed, offset,
-                                     draft_kind=kind_name(w["draft_kind"]))
+                                     draft_kind=kind_name(w["draft_kind"]), sibling_rule=RULE_NAMES[sibling_rule])
     torch.cuda.synchronize()
     return dict(tokens=ot.cpu().numpy(), count=oc.cpu().numpy(), path=op.cpu().numpy())
 
 
-def oracle_tree(w, seed=None, offset=None, rows=None):
+def oracle_tree(w, seed=None, offset=None, rows=None, sibling_rule=oracle.SIBLINGS_WOR):
     seed = w["seed"] if seed is None else seed
     offset = w["offset"] if offset is None else offset
     sel = slice(None) if rows is None else np.asarray(rows)
     rid = None if rows is None else np.asarray(rows, np.int32)
     return oracle.verify_tree(w["target"][sel], w["draft"][sel], w["node_tokens"][sel], w["parent"][sel],
                               w["temperature"][sel], w["max_depth"], seed, offset, draft_kind=w["draft_kind"],
-                              row_id=rid)
+                              row_id=rid, sibling_rule=sibling_rule)
 
 
 def compare(gpu, ora, rows=None, keys=("tokens", "count")):

@@ -8,6 +8,7 @@ import numpy as np
 sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 
+import oracle  # noqa: E402
 from speculative_decoding_verification_53_gb300 import synth  # noqa: E402
 from _harness import compare, gpu_chain, gpu_tree, oracle_chain, oracle_tree  # noqa: E402
 
@@ -30,6 +31,10 @@ def main():
     for T in (0.0, 1.0):
         tw["temperature"] = np.full(4, T, np.float32)
         excused += compare(gpu_tree(tw, seed=2), oracle_tree(tw, seed=2), keys=("tokens", "count", "path"))
+    iw = synth.redraw_children_iid(synth.tree(seed=16, B=4, N=24, V=8192, max_depth=5, sigma=2.0), seed=5)
+    for rule in (oracle.SIBLINGS_IID, oracle.SIBLINGS_WOR):
+        excused += compare(gpu_tree(iw, seed=7, sibling_rule=rule), oracle_tree(iw, seed=7, sibling_rule=rule),
+                           keys=("tokens", "count", "path"))
     cw = synth.chain_as_tree(synth.tiny_chain(seed=7, V=2048, K=6, B=8, temperature=0.8))
     excused += compare(gpu_tree(cw, seed=4), oracle_tree(cw, seed=4), keys=("tokens", "count", "path"))
     assert excused <= 2, excused

@@ -232,6 +232,49 @@ def test_bad_arguments_raise():
                              0, 0, draft_kind="logits")
 
 
+# ------------------------------------------------------ multi-draft siblings
+
+@pytest.mark.parametrize("rule", [oracle.SIBLINGS_IID, oracle.SIBLINGS_WOR])
+def test_tree_iid_children_both_rules_full_size(rule):
+    """Trees whose children were drafted i.i.d. from q (tokens may repeat among siblings),
+    V=128256, verified under either sibling rule, against the oracle under the same rule."""
+    w = synth.redraw_children_iid(synth.tree(seed=71, temperature=1.0, B=8), seed=3)
+    compare(gpu_tree(w, seed=5, sibling_rule=rule), oracle_tree(w, seed=5, sibling_rule=rule),
+            keys=("tokens", "count", "path"))
+
+
+def test_gpu_multidraft_law_with_iid_children():
+    """10^6 rounds of a root with three children drawn i.i.d. from q (V=16): with the i.i.d.
+    rule the first emitted token follows p (TV within the 99th percentile of an exact
+    sampler's TV); the without-replacement rule on the same drafts is visibly biased."""
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    V, C, B, calls = 16, 3, 62500, 16
+    rng = np.random.default_rng(43)
+    t = (rng.normal(0, 0.8, (C + 1, V))).astype(np.float32)
+    d = (t + rng.normal(0, 0.8, (C + 1, V))).astype(np.float32)
+    q = np.exp(d[0].astype(np.float64) - d[0].max())
+    q /= q.sum()
+    p = np.exp(t[0].astype(np.float64) - t[0].max())
+    p /= p.sum()
+    tt = to_dev(np.broadcast_to(t, (B, C + 1, V)).copy())
+    dd = to_dev(np.broadcast_to(d, (B, C + 1, V)).copy())
+    par = to_dev(np.full((B, C), -1, np.int32))
+    temps = torch.ones(B, device="cuda")
+    first = {"iid": [], "without_replacement": []}
+    for c in range(calls):
+        toks = to_dev(rng.choice(V, (B, C), p=q).astype(np.int32))
+        for rule in first:
+            ot, _, _ = sv.spec_verify_tree(tt, dd, toks, par, temps, 1, 2000 + c, c, draft_kind="logits",
+                                           sibling_rule=rule)
+            first[rule].append(ot[:, 0].cpu().numpy())
+    n = B * calls
+    exact = [0.5 * np.abs(rng.multinomial(n, p) / n - p).sum() for _ in range(300)]
+    tv = {r: 0.5 * np.abs(np.bincount(np.concatenate(v), minlength=V) / n - p).sum() for r, v in first.items()}
+    assert tv["iid"] <= np.quantile(exact, 0.99), tv
+    assert tv["without_replacement"] > 2 * np.quantile(exact, 0.99), tv
+
+
 # ----------------------------------------------------------- statistics
 
 def test_gpu_output_law_and_expected_count():
