@@ -530,22 +530,14 @@ struct DrawResult {
     int failed;  // some CTA reported fail_in (a staging wait that gave up): the draw is void
 };
 
+// The draw given the tile sums of this CTA's chunk (tile t: elements lo + 256 t ..);
+// wf evaluates the weights of the one tile the owner CTA searches.  The caller has
+// synchronised the CTA after writing tile_sum.
 template <class WF>
-__device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float* tile_sum, BlockScratch& sc,
-                                   int& phase, int fail_in = 0) {
+__device__ __forceinline__ DrawResult cluster_draw_from_tiles(const WF& wf, int lo, int hi, float u, const float* tile_sum,
+                                              BlockScratch& sc, int& phase, int fail_in = 0) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ntiles = (hi - lo + TILE - 1) / TILE;
-    for (int t = warp; t < ntiles; t += NW) {
-        float w[VEC];
-        wf.eval8(lo + t * TILE + lane * VEC, hi, w);
-        float s = 0.f;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) s += w[j];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) tile_sum[t] = s;
-    }
-    __syncthreads();
     if (warp == 0) {
         float z = 0.f;
         for (int t = lane; t < ntiles; t += 32) z += tile_sum[t];
@@ -666,6 +658,25 @@ __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float*
     res.token = sc.bi[2];
     __syncthreads();
     return res;
+}
+
+template <class WF>
+__device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float* tile_sum, BlockScratch& sc,
+                                   int& phase, int fail_in = 0) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ntiles = (hi - lo + TILE - 1) / TILE;
+    for (int t = warp; t < ntiles; t += NW) {
+        float w[VEC];
+        wf.eval8(lo + t * TILE + lane * VEC, hi, w);
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) s += w[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) tile_sum[t] = s;
+    }
+    __syncthreads();
+    return cluster_draw_from_tiles(wf, lo, hi, u, tile_sum, sc, phase, fail_in);
 }
 
 }  // namespace sv

@@ -91,6 +91,7 @@ cudaError_t launch_tree(const TreeArgs& a, int tdt, int ddt, int dk, int cluster
 // Dynamic shared memory (tile sums of the draw) for a row split `cluster` ways.
 size_t draw_smem_bytes(int V, int cluster);
 
+
 // Draft tokens x_k ~ softmax(draft_k / T) (argmax for greedy rows) for every (b, k).
 cudaError_t launch_draft_sample(const SampleArgs& a, int ddt, int num_sms, cudaStream_t stream);
 

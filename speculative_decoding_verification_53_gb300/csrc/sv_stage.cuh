@@ -60,12 +60,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; gives up after a bounded number
-// of polls (about a quarter of a second) and returns false.
+// try_wait with a suspend-time hint: the thread may be suspended in hardware (woken when
+// the phase completes) for up to `ns` nanoseconds instead of returning at once, so a
+// waiting warp does not spin through issue slots other warps could use.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete.  Gives up and returns false
+// after a quarter of a second (global timer) or 2^22 tries, whichever comes first.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
+    const uint64_t t0 = global_ns();
     for (uint32_t i = 0; i < (1u << 22); ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (i >= 32) __nanosleep(64);
+        if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
+        if (global_ns() - t0 > 250000000ull) break;
     }
     return false;
 }
