@@ -21,6 +21,7 @@ namespace sv {
 
 template <int TDT>
 struct PWeights {  // w_i = p_i (the bonus draw, or the fallback of an empty residual)
+    static constexpr int kTilesInFlight = 4;  // global loads: several in flight per lane
     const void* trow;
     float c, m, inv_s;
     bool al;
@@ -34,6 +35,7 @@ struct PWeights {  // w_i = p_i (the bonus draw, or the fallback of an empty res
 
 template <int TDT, int DDT, int DK>
 struct ResidualWeights {  // w_i = max(0, p_i - q_i)
+    static constexpr int kTilesInFlight = 4;  // global loads: several in flight per lane
     const void* trow;
     const void* drow;
     float c, mt, inv_st, md, inv_sd;
@@ -62,6 +64,8 @@ __global__ void __launch_bounds__(NT) chain_kernel(const ChainArgs a) {
     __shared__ int s_tok[MAX_K];
     __shared__ float s_r[MAX_K + 1], s_u[MAX_K + 1], s_ap[MAX_K];
 
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
     const int G = (int)cluster_size(), g = (int)cluster_rank();
     const int b = blockIdx.y;
     const int K = a.K, V = a.V;
@@ -185,13 +189,15 @@ static cudaError_t launch_chain_t(const ChainArgs& a, int G, cudaStream_t stream
     while (G > max_cluster) G >>= 1;
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
     cfg.dynamicSmemBytes = draw_smem_bytes(a.V, G);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

@@ -60,6 +60,8 @@ __device__ __forceinline__ void seg_argmax(float& v, int& i, int& nan, int width
 
 template <int TDT, int DDT, int DK>
 __global__ void __launch_bounds__(NT) chain_eager_kernel(const EagerArgs E) {
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
     const ChainArgs& a = E.a;
     extern __shared__ __align__(128) unsigned char dsm[];
     const int K = a.K, P = K + 1, V = a.V;
@@ -355,13 +357,15 @@ static cudaError_t launch_chain_eager_t(const ChainArgs& a, int G, cudaStream_t 
     }
     if (cached_max < G) return cudaErrorInvalidClusterSize;
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, E);
 }
 

@@ -137,10 +137,20 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
     // which this small-batch kernel accepts); the temperature, the tokens and the Philox
     // block are fetched and computed meanwhile, independently of each other
     const bool has_draft_row = k < K && a.draft != nullptr;
+    if (threadIdx.x == 32) {  // warp 1: the Philox block of slot k (unused on greedy rows)
+        float r, u;
+        slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, r, u);
+        s_flt[0] = r;
+        s_flt[1] = u;
+    }
     if (threadIdx.x == 0) {
         mbar_init(tbar, 1);
         mbar_init(dbar, 1);
         fence_mbar_init();
+    }
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
+    if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(tbar, (uint32_t)n * tsz);
         if (n) bulk_g2s(tb, trow + (size_t)lo * tsz, (uint32_t)n * tsz, tbar);
         if (has_draft_row) {
@@ -148,17 +158,18 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
             if (n) bulk_g2s(db, drow + (size_t)lo * dsz, (uint32_t)n * dsz, dbar);
         }
     }
+    // draft probabilities: only q(x_k) takes part in the statistics, so thread 0 fetches
+    // it directly and the q chunk (needed by the draw alone) keeps landing meanwhile
+    float qx_direct = 0.f;
+    if (DK == DK_PROBS && threadIdx.x == 0 && has_draft_row) {
+        const int xk = a.tokens[(size_t)b * K + k];
+        if (xk >= lo && xk < hi) qx_direct = load_one<DT_F32>(drow, xk);
+    }
     int tok_bad = 0;
     for (int i = threadIdx.x; i < K; i += NT) {
         const int x = a.tokens[(size_t)b * K + i];
         s_tok[i] = x;
         if (x < 0 || x >= V) tok_bad = 1;
-    }
-    if (threadIdx.x == 32) {  // warp 1: the Philox block of slot k (unused on greedy rows)
-        float r, u;
-        slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, r, u);
-        s_flt[0] = r;
-        s_flt[1] = u;
     }
     const float T = a.temperature ? a.temperature[b] : 0.f;
     const bool greedy = !(T > 0.f);
@@ -167,7 +178,11 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
 
     // 2. statistics of row k, the acceptance test of x_k
     bool ok = mbar_wait_bounded(tbar, 0);
-    if (has_draft_row) ok = mbar_wait_bounded(dbar, 0) && ok;
+    bool draft_landed = !has_draft_row;
+    if (has_draft_row && DK == DK_LOGITS) {  // draft logits feed the statistics
+        ok = mbar_wait_bounded(dbar, 0) && ok;
+        draft_landed = true;
+    }
     const int fail = __syncthreads_or(!ok);
     const int x = (k < K && !tokens_bad) ? s_tok[k] : -1;
     SpecRec* rec = reinterpret_cast<SpecRec*>(A.ws + A.wl.rec_off) + (size_t)b * (K + 1) + k;
@@ -189,7 +204,7 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
         int has = 0;
         if (threadIdx.x == 0 && x >= lo && x < hi) {
             tx = smem_elem<TDT>(tb, x - lo);
-            dx = (DK == DK_LOGITS) ? smem_elem<DDT>(db, x - lo) : smem_elem<DT_F32>(db, x - lo);
+            dx = (DK == DK_LOGITS) ? smem_elem<DDT>(db, x - lo) : qx_direct;
             has = 1;
         }
         const PosStats ps = cluster_pos_stats<DK == DK_LOGITS>(ts, ds, c, tx, dx, has, sc, phase);
@@ -208,8 +223,13 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
             const float u = s_flt[1];
             DrawResult d;
             if (k < K) {
+                int dfail = 0;
+                if (!draft_landed) {  // the q chunk, for the residual
+                    dfail = __syncthreads_or(!mbar_wait_bounded(dbar, 0));
+                    draft_landed = true;
+                }
                 const StagedResidual<TDT, DDT, DK> rw{tb, db, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd};
-                d = cluster_draw(rw, lo, hi, u, tile_sum, sc, phase);
+                d = cluster_draw(rw, lo, hi, u, tile_sum, sc, phase, dfail);
                 if (!d.failed && d.owner < 0) {  // the residual has no mass: draw from p_k
                     const StagedP<TDT> pw{tb, lo, c, ps.t.m, inv_st};
                     d = cluster_draw(pw, lo, hi, u, tile_sum, sc, phase);
@@ -223,6 +243,9 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
         }
         if (bad) flags |= SPEC_BAD;
     }
+    // a copy still in flight must land before the CTA exits (a greedy or invalid row
+    // never waited for its q chunk)
+    if (!draft_landed && threadIdx.x == 0) (void)mbar_wait_bounded(dbar, 0);
     // 4. publish the position record and count this CTA in
     if (g == 0 && threadIdx.x == 0) {
         rec->ratio = ratio;
@@ -298,13 +321,15 @@ static cudaError_t launch_chain_spec_t(const ChainArgs& a, void* ws, int G, cuda
     }
     if (cached_max < G) return cudaErrorInvalidClusterSize;
     cfg.gridDim = dim3((unsigned)G, (unsigned)(a.K + 1), (unsigned)a.B);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, A);
 }
 

@@ -58,11 +58,18 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
             bulk_g2s(slots + (size_t)s * L.slot_bytes + L.t_bytes, dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz,
                      &dbar[s]);
     };
+    // the Philox blocks (kernel parameters only) on warps 1.. before the dependency wait;
+    // greedy rows simply never use them
+    for (int k = (int)threadIdx.x - 32; k >= 0 && k <= K; k += NT - 32)
+        slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, s_r[k], s_u[k]);
     if (threadIdx.x == 0) {
         for (int i = 0; i <= 2 * L.nslot; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
-        for (int k = 0; k < first; ++k) issue_t(k);
     }
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
+    if (threadIdx.x == 0)
+        for (int k = 0; k < first; ++k) issue_t(k);
     const float T = a.temperature ? a.temperature[b] : 0.f;
     const bool greedy = !(T > 0.f);
     const float c = greedy ? 0.f : LOG2E / T;
@@ -86,10 +93,6 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
         s_ap[k] = -1.f;
         if (x < 0 || x >= V) tok_bad = 1;
     }
-    // Philox blocks on warps 1.. (warp 0 issues the copies), independent of the temperature
-    // so that they overlap the loads; greedy rows simply never use them
-    for (int k = (int)threadIdx.x - 32; k >= 0 && k <= K; k += NT - 32)
-        slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, s_r[k], s_u[k]);
     bool invalid = __syncthreads_or(tok_bad) != 0;
 
     auto issue = [&](int k) {  // refill: position k into slot k % nslot (its previous reads are done)
@@ -263,13 +266,15 @@ static cudaError_t launch_chain_staged_t(const ChainArgs& a, const StageLayout& 
     }
     if (cached_max < G) return cudaErrorInvalidClusterSize;  // caller picks another shape
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, a, L);
 }
 

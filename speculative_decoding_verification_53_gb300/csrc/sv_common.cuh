@@ -80,6 +80,15 @@ __device__ __forceinline__ void slot_uniforms(uint64_t seed, uint64_t offset, ui
     u = (float)(uint32_t)(x1 >> 40) * (1.0f / 16777216.0f);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization, so it may start while the previous kernel on the
+// stream (typically the one that produced the logits) is still finishing.  pdl_wait()
+// blocks until that kernel has completed and its writes are visible: it precedes every
+// read of an input and every write of an output or workspace.  pdl_trigger() lets the
+// next such kernel on the stream start its own launch early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // The draft-sampling uniform of a Philox slot: word 2, on the same 24-bit grid.
 __device__ __forceinline__ float slot_draft_uniform(uint64_t seed, uint64_t offset, uint64_t row, uint64_t slot) {
     uint64_t x0 = slot, x1 = row, x2 = offset, x3 = 0;
@@ -660,20 +669,43 @@ __device__ __forceinline__ DrawResult cluster_draw_from_tiles(const WF& wf, int 
     return res;
 }
 
+// Tiles a warp evaluates before reducing them: weight functors that read global memory
+// declare kTilesInFlight (several loads in flight per lane); shared-memory ones take 1.
+template <class T, class = void>
+struct TilesInFlight {
+    static constexpr int value = 1;
+};
+template <class T>
+struct TilesInFlight<T, decltype((void)T::kTilesInFlight)> {
+    static constexpr int value = T::kTilesInFlight;
+};
+
 template <class WF>
 __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float* tile_sum, BlockScratch& sc,
                                    int& phase, int fail_in = 0) {
+    constexpr int TB = TilesInFlight<WF>::value;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ntiles = (hi - lo + TILE - 1) / TILE;
-    for (int t = warp; t < ntiles; t += NW) {
-        float w[VEC];
-        wf.eval8(lo + t * TILE + lane * VEC, hi, w);
-        float s = 0.f;
+    for (int t0 = warp * TB; t0 < ntiles; t0 += NW * TB) {
+        float w[TB][VEC];
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) s += w[j];
+        for (int i = 0; i < TB; ++i) {
+            if (t0 + i < ntiles) {
+                wf.eval8(lo + (t0 + i) * TILE + lane * VEC, hi, w[i]);
+            } else {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) tile_sum[t] = s;
+                for (int j = 0; j < VEC; ++j) w[i][j] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < TB; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) s += w[i][j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0 && t0 + i < ntiles) tile_sum[t0 + i] = s;
+        }
     }
     __syncthreads();
     return cluster_draw_from_tiles(wf, lo, hi, u, tile_sum, sc, phase, fail_in);

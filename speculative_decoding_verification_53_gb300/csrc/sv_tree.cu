@@ -92,6 +92,8 @@ __device__ __forceinline__ bool tree_row_bad(const LSE& s) {
 
 template <int TDT, int DDT, int DK>
 __global__ void __launch_bounds__(NT) tree_kernel(const TreeArgs a) {
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
     extern __shared__ float tile_sum[];
     __shared__ BlockScratch sc;
     __shared__ int s_tok[MAX_NODES], s_par[MAX_NODES], s_child[MAX_NODES];
@@ -283,13 +285,15 @@ static cudaError_t launch_tree_t(const TreeArgs& a, int G, cudaStream_t stream) 
     while (G > max_cluster) G >>= 1;
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
     cfg.dynamicSmemBytes = draw_smem_bytes(a.V, G);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

@@ -26,9 +26,29 @@
 #include <cstdint>
 
 #include "spec_tree_kv.h"
+#include "sv_common.cuh"
 #include "sv_internal.h"
 
 namespace {
+
+using sv::pdl_trigger;
+using sv::pdl_wait;
+
+// A launch with programmatic stream serialization (the kernels call pdl_wait first).
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 constexpr int kMaskMaxN = 1024;
 constexpr int kKvMaxBuffers = 256;
@@ -82,6 +102,8 @@ __global__ void __launch_bounds__(1024, 2) tree_mask_kernel(const int32_t* __res
                                                             uint32_t* __restrict__ out_mask,
                                                             int32_t* __restrict__ out_depth,
                                                             int32_t* __restrict__ out_valid) {
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
     extern __shared__ __align__(16) uint32_t s_rows[];
     int* s_par = reinterpret_cast<int*>(s_rows + tri_off(N));
     int* s_dep = s_par + N;    // nodes from i up to its current jump target (finally: the depth)
@@ -256,6 +278,8 @@ __device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
 __global__ void __launch_bounds__(32 * kSmallMaskTreesPerCta) tree_mask_small_kernel(
     const int32_t* __restrict__ parent, int B, int N, int W, uint32_t* __restrict__ out_mask,
     int32_t* __restrict__ out_depth, int32_t* __restrict__ out_valid) {
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * kSmallMaskTreesPerCta + (threadIdx.x >> 5);
     if (b >= B) return;  // whole warps leave together
@@ -328,8 +352,7 @@ cudaError_t launch_mask(const int32_t* parent, int B, int N, int W, uint32_t* ma
                                              (int)smem);
         if (e != cudaSuccess) return e;
     }
-    tree_mask_kernel<CW><<<B, threads, smem, stream>>>(parent, N, W, mask, depth, valid);
-    return cudaGetLastError();
+    return launch_pdl(tree_mask_kernel<CW>, dim3(B), dim3(threads), smem, stream, parent, N, W, mask, depth, valid);
 }
 
 // ------------------------------------------------------------- KV compaction
@@ -352,6 +375,8 @@ template <> struct Piece<1> { using T = uint8_t; };
 // grid: x covers num_buffers * num_planes * pieces, y is the batch row.
 template <int PW>
 __global__ void __launch_bounds__(kKvThreads) kv_compact_kernel(const __grid_constant__ KvArgs a) {
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
     using T = typename Piece<PW>::T;
     __shared__ int s_dst[kKvMaxDepth], s_src[kKvMaxDepth];
     __shared__ int s_moves, s_base;
@@ -421,9 +446,8 @@ sv_status spec_tree_mask(const int32_t* parent, int B, int N, uint32_t* out_mask
     const int chunks = (W + 3) / 4;
     if (N <= 64) {
         const int grid = (B + kSmallMaskTreesPerCta - 1) / kSmallMaskTreesPerCta;
-        tree_mask_small_kernel<<<grid, 32 * kSmallMaskTreesPerCta, 0, s>>>(parent, B, N, W, out_mask, out_depth,
-                                                                          out_valid);
-        e = cudaGetLastError();
+        e = launch_pdl(tree_mask_small_kernel, dim3(grid), dim3(32 * kSmallMaskTreesPerCta), 0, s, parent, B, N, W,
+                       out_mask, out_depth, out_valid);
     } else if (chunks <= 1) e = launch_mask<1>(parent, B, N, W, out_mask, out_depth, out_valid, s);
     else if (chunks <= 2) e = launch_mask<2>(parent, B, N, W, out_mask, out_depth, out_valid, s);
     else if (chunks <= 4) e = launch_mask<4>(parent, B, N, W, out_mask, out_depth, out_valid, s);
@@ -464,10 +488,11 @@ sv_status spec_kv_compact(void* const* kv_buffers, int num_buffers, int64_t batc
     a.base = base;
     const dim3 grid((unsigned)((total + kKvThreads - 1) / kKvThreads), (unsigned)B);
     cudaStream_t s = (cudaStream_t)stream;
-    if (pw == 16) kv_compact_kernel<16><<<grid, kKvThreads, 0, s>>>(a);
-    else if (pw == 4) kv_compact_kernel<4><<<grid, kKvThreads, 0, s>>>(a);
-    else kv_compact_kernel<1><<<grid, kKvThreads, 0, s>>>(a);
-    return sv::launch_status(cudaGetLastError());
+    cudaError_t e;
+    if (pw == 16) e = launch_pdl(kv_compact_kernel<16>, grid, dim3(kKvThreads), 0, s, a);
+    else if (pw == 4) e = launch_pdl(kv_compact_kernel<4>, grid, dim3(kKvThreads), 0, s, a);
+    else e = launch_pdl(kv_compact_kernel<1>, grid, dim3(kKvThreads), 0, s, a);
+    return sv::launch_status(e);
 }
 
 }  // extern "C"

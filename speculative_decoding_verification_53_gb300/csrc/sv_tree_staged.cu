@@ -85,6 +85,8 @@ constexpr int TREE_GATHER = 64;  // children whose raw values are prefetched at 
 
 template <int TDT, int DDT, int DK>
 __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const StageLayout L) {
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
     extern __shared__ __align__(128) unsigned char dsm[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(dsm);  // one mbarrier per slot
     unsigned char* slots = dsm + STAGE_HEADER;
@@ -368,13 +370,15 @@ static cudaError_t launch_tree_staged_t(const TreeArgs& a, const StageLayout& L,
     }
     if (cached_max < G) return cudaErrorInvalidClusterSize;
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, a, Lk);
 }
 
