@@ -315,8 +315,10 @@ sv_status spec_verify_tree_rule(const void* target_logits, sv_dtype tdt, const v
         L.t_bytes = (int)round16(cmax * tsz);
         L.slot_bytes = L.t_bytes + (int)round16(cmax * dsz);
         const bool small = (long long)B * G <= info.sms;
-        const size_t budget = small ? (size_t)sv::MAX_DYN_SMEM - 48 * 1024 : (size_t)90 * 1024;
-        const size_t fixed = sv::STAGE_HEADER + sv::draw_smem_bytes(V, G);
+        // two CTAs a SM for a large batch (about 8 KB of static shared memory each)
+        const size_t budget = small ? (size_t)sv::MAX_DYN_SMEM - 16 * 1024 : (size_t)104 * 1024;
+        const size_t fixed = sv::STAGE_HEADER + sv::tree_array_bytes(N) + sv::tree_work_bytes(V, G) +
+                             sv::draw_smem_bytes(V, G);
         if (fixed + L.slot_bytes <= budget) {
             size_t nslot = (budget - fixed) / L.slot_bytes;
             if (nslot > 16) nslot = 16;

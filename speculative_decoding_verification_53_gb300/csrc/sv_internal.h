@@ -48,6 +48,27 @@ struct SampleArgs {
     int32_t* out_draft_tokens; // [B][K]
 };
 
+// Per-tree arrays of the staged tree kernel in dynamic shared memory (N nodes): tokens,
+// parents, children / depth counts, jump targets, accept uniforms (N each), draw
+// uniforms (N + 1) and the rejection history (tried token, applied flag: N each;
+// 1/Z and q scale: N + 1 each), rounded up to 128 bytes.
+__host__ __device__ inline size_t tree_array_bytes(int N) {
+    return ((size_t)(10 * N + 3) * 4 + 127) & ~(size_t)127;
+}
+
+// Largest chunk of a row a CTA of a G-CTA cluster owns (whole 8-element vectors).
+__host__ __device__ inline int chunk_cap(int V, int G) {
+    const int nvec = (V + 7) / 8;
+    return ((nvec + G - 1) / G) * 8;
+}
+
+// Working area of the staged tree kernel: the current weights (fp32, one chunk) and
+// the bitmask of tokens tried at the current node, 16-byte aligned.
+__host__ __device__ inline size_t tree_work_bytes(int V, int G) {
+    const size_t cap = (size_t)chunk_cap(V, G);
+    return ((cap * 4 + 15) & ~(size_t)15) + ((((cap + 31) / 32) * 4 + 15) & ~(size_t)15);
+}
+
 // Shared-memory layout of the staged chain kernel (host-computed per launch).
 struct StageLayout {
     int nslot;        // ring slots, one position's row chunks each (1..16)

@@ -5,38 +5,43 @@
 // of the current node are tried in index order; greedy rows descend into the
 // child whose token is the argmax; sampling rows keep child c with probability
 // min(1, p(t_c)/q(t_c)) and, after a rejection, continue with p <- (p - q)+/Z,
-// q(t_c) <- 0, q renormalised; with no child kept (or at a leaf) the last token
-// is drawn from the current p.
+// q(t_c) <- 0, q renormalised (i.i.d. siblings: q left as it is); with no child
+// kept (or at a leaf) the last token is drawn from the current p.
 //
-// Here each CTA's chunk of the current node's target and draft rows sits in a
-// shared-memory slot (bulk copy on an mbarrier), so every sibling-rejection pass
-// and the final draw read shared memory, and the children's rows are prefetched
-// into spare slots while the current node is decided: the descent finds its
-// next rows already on chip.  Rows of nodes that are neither on the walked path
-// nor children of it are never read.
+// Each CTA's chunk of the current node's target and draft rows sits in a
+// shared-memory slot (bulk copy on an mbarrier), and the children's rows are
+// prefetched into spare slots while the current node is decided.  The current
+// (unnormalised) weights w_h after h rejections are kept in an fp32 array of the
+// chunk and updated in place by each rejection pass, w_{h+1} = (w_h / Z_h - q_h)+,
+// so a pass and the final draw cost O(1) per element whatever the number of
+// rejections; the tokens tried so far are a bitmask of the chunk.  The acceptance
+// test of a child evaluates the same recursion for its one token from the
+// recorded history (the same operations in the same order, so both agree bit for
+// bit).  Rows of nodes that are neither on the walked path nor children of it
+// are never read.
 #include "sv_stage.cuh"
 #include "sv_internal.h"
 
 namespace sv {
 
+// Rejection history at the current node (views into shared memory).
 struct TreeHist {
-    int n;
-    int x[MAX_NODES];
-    float zinv[MAX_NODES + 1];
-    float qs[MAX_NODES + 1];
-    unsigned char applied[MAX_NODES];
+    int* x;          // token tried at step h (-1: none recorded, i.i.d. siblings)
+    float* zinv;     // 1/Z after h steps (index h); zinv[0] = 1
+    float* qs;       // q scale after h steps (index h); qs[0] = 1
+    int* applied;    // step h replaced p by the residual (its mass was > 0)
 };
 
-// w_n(i), q_n(i) of element i after the recorded rejections (see sv_tree.cu).
-__device__ __forceinline__ void hist_state(const TreeHist& hs, int i, float p0, float q0, float& w, float& q) {
+// w_n(i), q_n(i) of element i after n recorded rejections, from p0(i), q0(i).
+__device__ __forceinline__ void hist_state(const TreeHist& hs, int n, int i, float p0, float q0, float& w, float& q) {
     w = p0;
     bool tried = false;
-    for (int h = 1; h <= hs.n; ++h) {
+    for (int h = 1; h <= n; ++h) {
         const float qprev = tried ? 0.f : q0 * hs.qs[h - 1];
         if (hs.applied[h - 1]) w = fmaxf(w * hs.zinv[h - 1] - qprev, 0.f);
         tried |= (i == hs.x[h - 1]);
     }
-    q = tried ? 0.f : q0 * hs.qs[hs.n];
+    q = tried ? 0.f : q0 * hs.qs[n];
 }
 
 // p0 / q0 of 8 staged elements of the current node (row coordinates).
@@ -58,46 +63,35 @@ struct StagedNode {
     }
 };
 
-template <int TDT, int DDT, int DK>
-struct StagedNodeDraw {  // the current p of the node, w_n(i)
-    StagedNode<TDT, DDT, DK> row;
-    const TreeHist* hs;
+// The current p of the node for the draw: the kept weights after a rejection, else p0.
+template <int TDT>
+struct StagedNodeP {
+    const unsigned char* tb;
+    const float* wbuf;
+    int lo;
+    float c, mtc, inv_st;
+    bool mat;
     __device__ __forceinline__ void eval8(int e0, int hi, float w[VEC]) const {
-        if (hs->n == 0) {
-            float l[VEC];
-            smem_load8<TDT>(row.tb, e0 - row.lo, hi - row.lo, neg_inf(), l);
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) w[j] = ex2(fmaf(l[j], row.c, -row.mtc)) * row.inv_st;
+        if (mat) {
+            smem_load8<DT_F32>(reinterpret_cast<const unsigned char*>(wbuf), e0 - lo, hi - lo, 0.f, w);
             return;
         }
-        float p0[VEC], q0[VEC];
-        row.load(e0, hi, p0, q0);
+        float l[VEC];
+        smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-            float q;
-            hist_state(*hs, e0 + j, p0[j], q0[j], w[j], q);
-        }
+        for (int j = 0; j < VEC; ++j) w[j] = ex2(fmaf(l[j], c, -mtc)) * inv_st;
     }
 };
-
 
 constexpr int TREE_GATHER = 64;  // children whose raw values are prefetched at node entry
 
 template <int TDT, int DDT, int DK>
 __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const StageLayout L) {
-    pdl_trigger();
-    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
     extern __shared__ __align__(128) unsigned char dsm[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(dsm);  // one mbarrier per slot
-    unsigned char* slots = dsm + STAGE_HEADER;
-    float* tile_sum = reinterpret_cast<float*>(slots + (size_t)L.nslot * L.slot_bytes);
     __shared__ BlockScratch sc;
-    __shared__ int s_tok[MAX_NODES], s_par[MAX_NODES], s_child[MAX_NODES];
-    __shared__ float s_r[MAX_NODES], s_u[MAX_NODES + 1];
     __shared__ float s_rt[TREE_GATHER], s_rd[TREE_GATHER];
     __shared__ int s_out[65], s_path[64];
-    __shared__ int s_nchild, s_flag;
-    __shared__ TreeHist hs;
+    __shared__ int s_nchild, s_hn;
 
     const int G = (int)cluster_size(), g = (int)cluster_rank();
     const int b = blockIdx.y;
@@ -109,6 +103,40 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
     const unsigned char* tbase = reinterpret_cast<const unsigned char*>(a.target) + (size_t)b * (N + 1) * V * tsz;
     const unsigned char* dbase = reinterpret_cast<const unsigned char*>(a.draft) + (size_t)b * (N + 1) * V * dsz;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    // dynamic shared memory: barriers | per-tree arrays | slots | weights, tried mask | tile sums
+    uint64_t* bars = reinterpret_cast<uint64_t*>(dsm);  // one mbarrier per slot
+    int* s_tok = reinterpret_cast<int*>(dsm + STAGE_HEADER);
+    int* s_par = s_tok + N;
+    int* s_child = s_par + N;  // depth counts first, then the children of the current node
+    int* s_jump = s_child + N;
+    float* s_r = reinterpret_cast<float*>(s_jump + N);
+    float* s_u = s_r + N;  // N + 1
+    int* h_x = reinterpret_cast<int*>(s_u + N + 1);
+    float* h_zinv = reinterpret_cast<float*>(h_x + N);  // N + 1
+    float* h_qs = h_zinv + N + 1;                         // N + 1
+    int* h_applied = reinterpret_cast<int*>(h_qs + N + 1);
+    const TreeHist hs{h_x, h_zinv, h_qs, h_applied};
+    unsigned char* slots = dsm + STAGE_HEADER + tree_array_bytes(N);
+    const int cap = chunk_cap(V, G);
+    float* wbuf = reinterpret_cast<float*>(slots + (size_t)L.nslot * L.slot_bytes);
+    uint32_t* tmask = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(wbuf) +
+                                                  (((size_t)cap * 4 + 15) & ~(size_t)15));
+    float* tile_sum = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(wbuf) + tree_work_bytes(V, G));
+
+    // barriers and the Philox blocks (kernel parameters only) before the dependency wait
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L.nslot; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    for (int i = (int)threadIdx.x - 32; i >= 0 && i <= N; i += NT - 32) {  // warps 1..
+        float r, u;
+        slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)i, r, u);
+        if (i < N) s_r[i] = r;
+        s_u[i] = u;
+    }
+    pdl_trigger();
+    pdl_wait();  // nothing the previous kernel on the stream writes is read before this
 
     // slot bookkeeping, identical in every thread: the row a slot holds (-1 free), copies in flight
     int slot_row[16];
@@ -139,10 +167,6 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
     };
 
     // the root's rows are requested first
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < L.nslot; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
     issue_t(0, 0);
     slot_row[0] = 0;
     pend = 1u;
@@ -151,13 +175,9 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
         const int t = a.node_tokens[(size_t)b * N + i], p = a.parent[(size_t)b * N + i];
         s_tok[i] = t;
         s_par[i] = p;
+        s_child[i] = 1;
+        s_jump[i] = p;
         if (t < 0 || t >= V || p < -1 || p >= i) bad = 1;
-    }
-    for (int i = (int)threadIdx.x - 32; i >= 0 && i <= N; i += NT - 32) {  // Philox blocks (warps 1..)
-        float r, u;
-        slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)i, r, u);
-        if (i < N) s_r[i] = r;
-        s_u[i] = u;
     }
     const float T = a.temperature[b];
     const bool greedy = !(T > 0.f);
@@ -165,19 +185,47 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
     const bool with_draft = !greedy;
     complete_issue(0, 0, with_draft);
     bool invalid = __syncthreads_or(bad) != 0;
-    if (!invalid && threadIdx.x == 0) {  // every node's depth must fit max_depth
-        int deep = 0;
-        for (int i = 0; i < N; ++i) {
-            const int p = s_par[i];
-            const int d = p < 0 ? 1 : s_child[p] + 1;  // s_child doubles as depth scratch here
-            s_child[i] = d;
-            if (d > D) deep = 1;
+    if (!invalid) {
+        // every node's depth must fit max_depth: depths by pointer jumping on (count, target)
+        // pairs, read / barrier / write rounds; a node stops at the root or beyond D
+        constexpr int PER = MAX_NODES / NT;
+        int dcur[PER], jcur[PER];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int i = (int)threadIdx.x + q * NT;
+            dcur[q] = 1;
+            jcur[q] = i < N ? s_par[i] : -1;
         }
-        s_flag = deep;
+        auto live = [&](int q) { return jcur[q] >= 0 && dcur[q] <= D; };
+        for (;;) {
+            int any = 0;
+#pragma unroll
+            for (int q = 0; q < PER; ++q) any |= live(q) ? 1 : 0;
+            if (!__syncthreads_or(any)) break;
+            int dd[PER], jj[PER];
+            bool act[PER];
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                act[q] = live(q);
+                dd[q] = act[q] ? s_child[jcur[q]] : 0;
+                jj[q] = act[q] ? s_jump[jcur[q]] : -1;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                if (!act[q]) continue;
+                const int i = (int)threadIdx.x + q * NT;
+                dcur[q] += dd[q];
+                jcur[q] = jj[q];
+                s_child[i] = dcur[q];
+                s_jump[i] = jcur[q];
+            }
+        }
+        int deep = 0;
+#pragma unroll
+        for (int q = 0; q < PER; ++q) deep |= dcur[q] > D ? 1 : 0;
+        invalid = __syncthreads_or(deep) != 0;
     }
-    __syncthreads();
-    if (!invalid) invalid = s_flag != 0;
-    __syncthreads();
 
     int phase = 0, emitted = 0, cur = -1, writer = 0, s_cur = 0;
     while (!invalid) {
@@ -195,11 +243,14 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
         }
         __syncthreads();
         const int nchild = s_nchild;
-        // raw values of the children's tokens in this node's rows (sampling), fetched while the copy lands
-        if (!greedy && (int)threadIdx.x < nchild && threadIdx.x < TREE_GATHER) {
+        // raw values of the children's tokens in this node's rows (sampling): the loads are
+        // issued now and their values stored after the statistics, so the latency overlaps
+        const bool gat = !greedy && (int)threadIdx.x < nchild && threadIdx.x < TREE_GATHER;
+        float g_rt = 0.f, g_rd = 0.f;
+        if (gat) {
             const int x = s_tok[s_child[threadIdx.x]];
-            s_rt[threadIdx.x] = load_one<TDT>(tbase + (size_t)row * V * tsz, x);
-            s_rd[threadIdx.x] = load_one<DDT>(dbase + (size_t)row * V * dsz, x);
+            g_rt = load_one<TDT>(tbase + (size_t)row * V * tsz, x);
+            g_rd = load_one<DDT>(dbase + (size_t)row * V * dsz, x);
         }
         // prefetch the children's rows into free slots
         for (int q = 0; q < nchild; ++q) {
@@ -233,17 +284,24 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
             LSE ds{neg_inf(), 0.f, 0};
             if (DK == DK_LOGITS && nchild > 0) ds = smem_thread_lse<DDT>(db, n, c);
             if (fail) ts.bad = 1;
+            if (gat) {
+                s_rt[threadIdx.x] = g_rt;
+                s_rd[threadIdx.x] = g_rd;
+            }
+            for (int w = threadIdx.x; w < (cap + 31) / 32; w += NT) tmask[w] = 0u;  // nothing tried yet
+            if (threadIdx.x == 0) {
+                s_hn = 0;
+                h_zinv[0] = 1.f;
+                h_qs[0] = 1.f;
+            }
+            // (the combine's barriers publish the gathered values, the mask and the history)
             const PosStats ps = cluster_pos_stats<DK == DK_LOGITS>(ts, ds, c, 0.f, 0.f, 0, sc, phase);
             if (row_bad_s(ps.t) || (DK == DK_LOGITS && nchild > 0 && row_bad_s(ps.d))) { invalid = true; break; }
             const float inv_st = 1.f / ps.t.s;
             const float inv_sd = (DK == DK_LOGITS && nchild > 0) ? 1.f / ps.d.s : 0.f;
             const StagedNode<TDT, DDT, DK> node{tb, db, lo, c, ps.t.m * c, inv_st, ps.d.m * c, inv_sd};
-            if (threadIdx.x == 0) {
-                hs.n = 0;
-                hs.zinv[0] = 1.f;
-                hs.qs[0] = 1.f;
-            }
-            __syncthreads();
+            const bool iid = a.sibling_rule == SV_SIBLINGS_IID;
+            bool wmat = false;  // wbuf holds w_h (else the current weights are still p0)
             for (int q = 0; q < nchild && !invalid; ++q) {
                 const int cidx = s_child[q], x = s_tok[cidx];
                 const float rt = q < TREE_GATHER ? s_rt[q] : load_one<TDT>(tbase + (size_t)row * V * tsz, x);
@@ -251,42 +309,81 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
                 const float p0x = ex2(fmaf(rt, c, -node.mtc)) * inv_st;
                 const float q0x = (DK == DK_LOGITS) ? ex2(fmaf(rd, c, -node.mdc)) * inv_sd : rd;
                 if (DK == DK_PROBS && (!(q0x >= 0.f) || q0x == pos_inf())) { invalid = true; break; }
+                const int nh = s_hn;
                 float wx, qx;
-                hist_state(hs, x, p0x, q0x, wx, qx);
-                const float px = wx * hs.zinv[hs.n];
+                hist_state(hs, nh, x, p0x, q0x, wx, qx);
+                const float px = wx * h_zinv[nh];
                 const float ratio = qx > 0.f ? px / qx : (px > 0.f ? pos_inf() : 0.f);
                 if (s_r[cidx] < ratio) { next = cidx; break; }
-                // rejected: the next residual mass and q normaliser, from the staged chunk
+                // rejected: w_{h+1} = (w_h / Z_h - q_h)+ in place, with the residual mass and
+                // the mass of q without x
+                const float zi = h_zinv[nh], qsn = h_qs[nh];
                 float2 part = make_float2(0.f, 0.f);
-                const int nh = hs.n;
                 for (int e0 = lo + (int)threadIdx.x * VEC; e0 < hi; e0 += NT * VEC) {
-                    float p0[VEC], q0[VEC];
-                    node.load(e0, hi, p0, q0);
+                    const int o = e0 - lo;
+                    float wv[VEC], d[VEC];
+                    smem_load8<DDT>(db, o, n, DK == DK_LOGITS ? neg_inf() : 0.f, d);
+                    if (wmat) {
+                        smem_load8<DT_F32>(reinterpret_cast<const unsigned char*>(wbuf), o, n, 0.f, wv);
+                    } else {
+                        float l[VEC];
+                        smem_load8<TDT>(tb, o, n, neg_inf(), l);
 #pragma unroll
-                    for (int jj = 0; jj < VEC; ++jj) {
-                        float w, qq;
-                        hist_state(hs, e0 + jj, p0[jj], q0[jj], w, qq);
-                        part.x += fmaxf(w * hs.zinv[nh] - qq, 0.f);
-                        part.y += (e0 + jj == x) ? 0.f : qq;
+                        for (int j = 0; j < VEC; ++j) wv[j] = ex2(fmaf(l[j], c, -node.mtc)) * inv_st;
+                    }
+                    const uint32_t tw = tmask[o >> 5] >> (o & 31);  // 8 elements share a mask word
+                    float r[VEC];
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        const float q0 = (DK == DK_LOGITS) ? ex2(fmaf(d[j], c, -node.mdc)) * inv_sd : d[j];
+                        const float qq = ((tw >> j) & 1u) ? 0.f : q0 * qsn;
+                        r[j] = fmaxf(wv[j] * zi - qq, 0.f);
+                        part.x += r[j];
+                        part.y += (e0 + j == x) ? 0.f : qq;
+                    }
+                    if (o + VEC <= n) {
+                        *reinterpret_cast<float4*>(wbuf + o) = make_float4(r[0], r[1], r[2], r[3]);
+                        *reinterpret_cast<float4*>(wbuf + o + 4) = make_float4(r[4], r[5], r[6], r[7]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j)
+                            if (o + j < n) wbuf[o + j] = r[j];
                     }
                 }
                 const float2 tot = cluster_sum2(part, sc, phase);
                 if (threadIdx.x == 0) {
                     // without replacement the tried token leaves q and q is renormalised;
                     // i.i.d. siblings leave q as it is (no token recorded, no rescale)
-                    const bool iid = a.sibling_rule == SV_SIBLINGS_IID;
-                    hs.x[nh] = iid ? -1 : x;
-                    hs.applied[nh] = tot.x > 0.f ? 1 : 0;
-                    hs.zinv[nh + 1] = tot.x > 0.f ? 1.f / tot.x : hs.zinv[nh];
-                    hs.qs[nh + 1] = (!iid && tot.y > 0.f) ? hs.qs[nh] / tot.y : hs.qs[nh];
-                    hs.n = nh + 1;
+                    h_x[nh] = iid ? -1 : x;
+                    h_applied[nh] = tot.x > 0.f ? 1 : 0;
+                    h_zinv[nh + 1] = tot.x > 0.f ? 1.f / tot.x : zi;
+                    h_qs[nh + 1] = (!iid && tot.y > 0.f) ? qsn / tot.y : qsn;
+                    s_hn = nh + 1;
+                    if (!iid && x >= lo && x < hi) tmask[(x - lo) >> 5] |= 1u << ((x - lo) & 31);
                 }
                 __syncthreads();
+                if (tot.x > 0.f) {
+                    wmat = true;
+                } else if (wmat) {
+                    // the residual had no mass, so w stays w_h, which the pass overwrote:
+                    // rebuild it from the history (the pages' rule keeps p in this case)
+                    for (int e0 = lo + (int)threadIdx.x * VEC; e0 < hi; e0 += NT * VEC) {
+                        float p0[VEC], q0[VEC];
+                        node.load(e0, hi, p0, q0);
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            float w, qq;
+                            hist_state(hs, nh + 1, e0 + j, p0[j], q0[j], w, qq);
+                            if (e0 + j < hi) wbuf[e0 - lo + j] = w;
+                        }
+                    }
+                    __syncthreads();
+                }
             }
             if (invalid) break;
             if (next < 0) {  // no child kept (or a leaf): the last token from the current p
-                const StagedNodeDraw<TDT, DDT, DK> dw{node, &hs};
-                const DrawResult d = cluster_draw(dw, lo, hi, s_u[row], tile_sum, sc, phase);
+                const StagedNodeP<TDT> pw{tb, wbuf, lo, c, node.mtc, inv_st, wmat};
+                const DrawResult d = cluster_draw(pw, lo, hi, s_u[row], tile_sum, sc, phase);
                 if (threadIdx.x == 0) s_out[emitted] = d.token;
                 ++emitted;
                 writer = d.owner;
@@ -348,7 +445,8 @@ static cudaError_t launch_tree_staged_t(const TreeArgs& a, const StageLayout& L,
         max_dyn = m;
     }
     StageLayout Lk = L;
-    size_t smem = STAGE_HEADER + (size_t)Lk.nslot * Lk.slot_bytes + draw_smem_bytes(a.V, G);
+    size_t smem = STAGE_HEADER + tree_array_bytes(a.N) + (size_t)Lk.nslot * Lk.slot_bytes + tree_work_bytes(a.V, G) +
+                  draw_smem_bytes(a.V, G);
     while (smem > (size_t)max_dyn && Lk.nslot > 1) {  // fewer prefetch slots when static memory is large
         --Lk.nslot;
         smem -= Lk.slot_bytes;
