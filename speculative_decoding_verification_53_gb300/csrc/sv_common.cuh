@@ -326,12 +326,6 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
     return remote;
 }
 
-__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // Fire-and-forget store into a peer CTA's shared memory (ordered by the next
 // barrier.cluster release/acquire pair).
 __device__ __forceinline__ void dsmem_st_v4(uint32_t addr, float4 v) {
@@ -344,24 +338,6 @@ __device__ __forceinline__ void dsmem_st_v2(uint32_t addr, float2 v) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
 }
 
-__device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-// Per-CTA exchange record published to the cluster (double-buffered by phase).
-struct Xchg {
-    float f[8];
-    int i[4];
-};
-
-// Shared state of a CTA used by the block- and cluster-level reductions.
-// One warp's (max, sum) partials of the target and draft rows, published to the cluster.
-struct WarpPart {
-    float tm, ts, dm, ds;
-    int bad;  // bit 0: target row NaN, bit 1: draft row NaN
-};
 
 // Inbox of pushed partials: every warp of every CTA of the cluster stores its
 // (target max, target sum, draft max, draft sum) here with a remote store, so after
@@ -373,10 +349,9 @@ struct Inbox {
     float2 zf[2][MAX_CLUSTER];    // the draw's per-CTA total weight and failure flag
 };
 
+// Shared state of a CTA used by the block- and cluster-level reductions.
 struct BlockScratch {
-    Xchg xchg[2];
     Inbox inbox;
-    WarpPart wp[2][NW];
     float rf[NW][4];
     int ri[NW][2];
     float bf[8];  // broadcast floats
@@ -393,9 +368,12 @@ __device__ __forceinline__ void chunk_range(int V, int g, int G, int& lo, int& h
 }
 
 // Block reduce of up to two LSE pairs, then a cluster-wide combine in rank order.
-// Every thread of every CTA returns the same values.
+// Every thread of every CTA returns the same values.  Push model: warp 0 stores the
+// CTA's pairs into every peer's inbox, one cluster barrier, then a local combine.
 __device__ __forceinline__ void cluster_lse2(LSE& a, LSE& b, float c, BlockScratch& sc, int& phase) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t G = cluster_size(), me = cluster_rank();
+    const int buf = phase & 1;
     lse_warp_reduce(a, c);
     lse_warp_reduce(b, c);
     if (lane == 0) {
@@ -404,7 +382,6 @@ __device__ __forceinline__ void cluster_lse2(LSE& a, LSE& b, float c, BlockScrat
         sc.ri[warp][0] = a.bad; sc.ri[warp][1] = b.bad;
     }
     __syncthreads();
-    Xchg& slot = sc.xchg[phase & 1];
     if (warp == 0) {
         LSE x{neg_inf(), 0.f, 0}, y{neg_inf(), 0.f, 0};
         if (lane < NW) {
@@ -413,22 +390,20 @@ __device__ __forceinline__ void cluster_lse2(LSE& a, LSE& b, float c, BlockScrat
         }
         lse_warp_reduce(x, c);
         lse_warp_reduce(y, c);
-        if (lane == 0) {
-            slot.f[0] = x.m; slot.f[1] = x.s; slot.f[2] = y.m; slot.f[3] = y.s;
-            slot.i[0] = x.bad; slot.i[1] = y.bad;
+        if ((uint32_t)lane < G) {
+            const uint32_t peer = (uint32_t)lane;
+            dsmem_st_v4(dsmem_addr(&sc.inbox.part[buf][me][0], peer), make_float4(x.m, x.s, y.m, y.s));
+            dsmem_st_v4(dsmem_addr(&sc.inbox.part[buf][me][1], peer),
+                        make_float4(__int_as_float(x.bad), __int_as_float(y.bad), 0.f, 0.f));
         }
     }
     cluster_sync_all();
     if (warp == 0) {
-        const uint32_t G = cluster_size();
         LSE x{neg_inf(), 0.f, 0}, y{neg_inf(), 0.f, 0};
         if ((uint32_t)lane < G) {
-            x.m = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
-            x.s = dsmem_ld_f32(dsmem_addr(&slot.f[1], lane));
-            y.m = dsmem_ld_f32(dsmem_addr(&slot.f[2], lane));
-            y.s = dsmem_ld_f32(dsmem_addr(&slot.f[3], lane));
-            x.bad = dsmem_ld_s32(dsmem_addr(&slot.i[0], lane));
-            y.bad = dsmem_ld_s32(dsmem_addr(&slot.i[1], lane));
+            const float4 v = sc.inbox.part[buf][lane][0], f = sc.inbox.part[buf][lane][1];
+            x = LSE{v.x, v.y, __float_as_int(f.x)};
+            y = LSE{v.z, v.w, __float_as_int(f.y)};
         }
         lse_warp_reduce(x, c);
         lse_warp_reduce(y, c);
@@ -475,9 +450,13 @@ __device__ __forceinline__ ArgMax cluster_argmax(ArgMax a, BlockScratch& sc, int
     return r;
 }
 
-// Cluster-wide sum of two floats (fixed order, identical in every CTA).
+// Cluster-wide sum of two floats (fixed order, identical in every CTA).  Push model:
+// warp 0 stores the CTA's pair into every peer's inbox, one cluster barrier, then
+// each CTA adds its own inbox in rank order.
 __device__ __forceinline__ float2 cluster_sum2(float2 v, BlockScratch& sc, int& phase) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t G = cluster_size(), me = cluster_rank();
+    const int buf = phase & 1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
@@ -485,7 +464,6 @@ __device__ __forceinline__ float2 cluster_sum2(float2 v, BlockScratch& sc, int& 
     }
     if (lane == 0) { sc.rf[warp][0] = v.x; sc.rf[warp][1] = v.y; }
     __syncthreads();
-    Xchg& slot = sc.xchg[phase & 1];
     if (warp == 0) {
         float2 x = make_float2(0.f, 0.f);
         if (lane < NW) x = make_float2(sc.rf[lane][0], sc.rf[lane][1]);
@@ -494,16 +472,12 @@ __device__ __forceinline__ float2 cluster_sum2(float2 v, BlockScratch& sc, int& 
             x.x += __shfl_xor_sync(0xffffffffu, x.x, o);
             x.y += __shfl_xor_sync(0xffffffffu, x.y, o);
         }
-        if (lane == 0) { slot.f[0] = x.x; slot.f[1] = x.y; }
+        if ((uint32_t)lane < G) dsmem_st_v2(dsmem_addr(&sc.inbox.zf[buf][me], (uint32_t)lane), x);
     }
     cluster_sync_all();
     if (warp == 0) {
-        const uint32_t G = cluster_size();
         float2 x = make_float2(0.f, 0.f);
-        if ((uint32_t)lane < G) {
-            x.x = dsmem_ld_f32(dsmem_addr(&slot.f[0], lane));
-            x.y = dsmem_ld_f32(dsmem_addr(&slot.f[1], lane));
-        }
+        if ((uint32_t)lane < G) x = sc.inbox.zf[buf][lane];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             x.x += __shfl_xor_sync(0xffffffffu, x.x, o);

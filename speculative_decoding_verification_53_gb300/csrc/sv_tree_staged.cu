@@ -243,16 +243,8 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
         }
         __syncthreads();
         const int nchild = s_nchild;
-        // raw values of the children's tokens in this node's rows (sampling): the loads are
-        // issued now and their values stored after the statistics, so the latency overlaps
-        const bool gat = !greedy && (int)threadIdx.x < nchild && threadIdx.x < TREE_GATHER;
-        float g_rt = 0.f, g_rd = 0.f;
-        if (gat) {
-            const int x = s_tok[s_child[threadIdx.x]];
-            g_rt = load_one<TDT>(tbase + (size_t)row * V * tsz, x);
-            g_rd = load_one<DDT>(dbase + (size_t)row * V * dsz, x);
-        }
-        // prefetch the children's rows into free slots
+        // prefetch the children's rows into free slots (before the gathers below: the proxy
+        // fence of a copy would otherwise wait for thread 0's outstanding loads)
         for (int q = 0; q < nchild; ++q) {
             int s = -1;
             for (int t = 0; t < L.nslot; ++t)
@@ -265,6 +257,15 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
             complete_issue(crow, s, with_draft);
             slot_row[s] = crow;
             pend |= 1u << s;
+        }
+        // raw values of the children's tokens in this node's rows (sampling): the loads are
+        // issued now and their values stored after the statistics, so the latency overlaps
+        const bool gat = !greedy && (int)threadIdx.x < nchild && threadIdx.x < TREE_GATHER;
+        float g_rt = 0.f, g_rd = 0.f;
+        if (gat) {
+            const int x = s_tok[s_child[threadIdx.x]];
+            g_rt = load_one<TDT>(tbase + (size_t)row * V * tsz, x);
+            g_rd = load_one<DDT>(dbase + (size_t)row * V * dsz, x);
         }
         const int fail = __syncthreads_or((pend & (1u << s_cur)) ? !wait_slot(s_cur) : 0);
         const unsigned char* tb = slots + (size_t)s_cur * L.slot_bytes;
