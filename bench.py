@@ -120,10 +120,12 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(workload: str):
+def profile_traffic(workload: str, default_size: bool = True):
     """DRAM bytes per launch of the timed kernel from the committed ncu summary for this
     workload (profiles/<kernel>_<workload>.md), if the kernel sources still hash to the
-    value recorded there; else None.  Returns (bytes, summary path, kernel name)."""
+    value recorded there and the run uses the workload's default size and temperature
+    (the summaries describe that configuration); else None.  Returns (bytes, summary
+    path, kernel name)."""
     import glob
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"*_{workload}.md"))):
         text = open(path).read()
@@ -131,7 +133,7 @@ def profile_traffic(workload: str):
         hm = re.search(r"^kernel_source_sha:\s*([0-9a-f]+)", text, re.M)
         km = re.search(r"^kernel:\s*(\S+)", text, re.M)
         kernel = km.group(1) if km else None
-        if not m or not hm or hm.group(1) != kernel_source_hash():
+        if not m or not hm or hm.group(1) != kernel_source_hash() or not default_size:
             return None, os.path.relpath(path, ROOT), kernel
         return float(m.group(1)), os.path.relpath(path, ROOT), kernel
     return None, None, None
@@ -359,7 +361,8 @@ def run_ours(args, rank, world, device):
         return None
     peak, peak_src = measured_peak()
     achieved = bytes_per_launch / (ms_per_step / 1e3) / 1e9
-    traffic, prof, prof_kernel = profile_traffic(args.workload)
+    traffic, prof, prof_kernel = profile_traffic(args.workload, default_size=not (args.batch or args.temperature is not None
+                                                                               or args.rounds != 64))
     line = {
         "metric": METRIC,
         "value": value,
@@ -653,7 +656,7 @@ def run_aux(args, rank, world, device):
         return None
     peak, peak_src = measured_peak()
     achieved = bytes_per_launch / (ms_per_step / 1e3) / 1e9
-    traffic, prof, prof_kernel = profile_traffic(args.workload)
+    traffic, prof, prof_kernel = profile_traffic(args.workload, default_size=not (args.batch or args.nodes))
     return {
         "metric": a["metric"], "value": value, "unit": a["unit"], "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
