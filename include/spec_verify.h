@@ -124,7 +124,7 @@ SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt,
  * memory arena, a plugin interface that passes only input and output buffers) or a
  * path on which no allocation call is allowed.  Same arguments and outputs as
  * spec_verify_chain, minus the workspace.  Where it applies (small batches, aligned
- * rows) it runs the position-parallel kernel, whose scratch is a 2 MiB array inside
+ * rows) it runs the position-parallel kernel, whose scratch is a 256 KiB array inside
  * the library's device image, present on every device that loads the library until
  * the process exits; otherwise it runs the kernels that need no scratch.  Results
  * agree with spec_verify_chain except where a decision lies within fp32 rounding of
@@ -132,8 +132,8 @@ SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt,
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress, with the device current) and zeroes it synchronously;
  *     make that first call before any stream capture.
- *   - Calls whose scratch would exceed 2 MiB (spec_verify_workspace_size(B, K, V) >
- *     2 MiB) return SV_ERR_UNSUPPORTED without launching anything.
+ *   - Calls whose scratch would exceed 256 KiB (spec_verify_workspace_size(B, K, V) >
+ *     256 KiB) return SV_ERR_UNSUPPORTED without launching anything.
  *   - Every call shares the one array: calls that overlap on the GPU (different
  *     streams, or different host threads) race and must be serialised by the caller.
  */

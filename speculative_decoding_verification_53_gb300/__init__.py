@@ -195,7 +195,7 @@ def spec_verify_chain_noalloc(target_logits, draft, draft_tokens, temperature, s
                               draft_kind, out_tokens=None, out_count=None, out_accept_prob=None,
                               want_accept_prob: bool = False, stream=None):
     """spec_verify_chain for callers that cannot provide a workspace: the library uses a
-    fixed 2 MiB scratch array of its own (first call on a device sets it up, so make it
+    fixed 256 KiB scratch array of its own (first call on a device sets it up, so make it
     before any graph capture; overlapping calls race).  Same arguments and results."""
     torch = _torch()
     _dev(target_logits, "target_logits")

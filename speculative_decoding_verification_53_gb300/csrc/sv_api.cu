@@ -146,7 +146,8 @@ sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_
             (void)cudaGetLastError();
         }
     }
-    if ((path == PATH_AUTO || path == PATH_SPEC) && aligned && ws && ((uintptr_t)ws & 255u) == 0) {
+    if ((path == PATH_AUTO || path == PATH_SPEC) && aligned && ws && ((uintptr_t)ws & 255u) == 0 &&
+        a.K + 1 <= sv::SPEC_MAX_POS) {
         const int Gs = spec_cluster(a.B, a.K, num_sms);
         if ((path == PATH_SPEC || Gs >= 4) && ws_bytes >= sv::spec_workspace_bytes(a.B, a.K, a.V, Gs)) {
             const cudaError_t e = sv::launch_chain_spec(a, ws, tdt, ddt, dk, Gs, stream);

@@ -8,46 +8,43 @@
 // gets its own cluster of G CTAs at once:
 //   1. the cluster stages its chunk of target row k (and draft row k), computes
 //      the softmax statistics and the acceptance test of x_k (greedy: the argmax);
-//   2. it completes, speculatively, the draw at k as if k were the first
-//      rejection (the replacement from (p_k - q_k)+, or from p_k when that residual
-//      is empty; the bonus token from p_K at k = K), inside the cluster and from
-//      shared memory;
-//   3. it publishes a small per-position record (flags, ratio, drawn token) and
-//      counts itself in with one atomic.
+//   2. if x_k is rejected (or k = K), it completes the draw at k as if k were the
+//      first rejection (the replacement from (p_k - q_k)+, or from p_k when that
+//      residual is empty; the bonus token from p_K at k = K), inside the cluster
+//      and from shared memory;
+//   3. it writes output slot k itself (x_k when accepted, else the drawn token)
+//      and counts itself in with one 64-bit atomic that also carries the
+//      position's reject and invalid bits.
 // The last CTA to arrive for batch row b (no CTA ever waits for another) reads
-// the K+1 records, finds the first rejection j and writes the outputs.  The
-// results are those of the left-to-right rule; the price of the shorter
-// critical path is that positions past the first rejection are read and drawn
-// for nothing.
+// the first rejection j and the invalid bits off the value its own atomic
+// returned, clears the slots after j and writes the count.  The results are
+// those of the left-to-right rule; the price of the shorter critical path is that
+// positions past the first rejection are read (and their draws made) for nothing.
 #include "sv_stage.cuh"
 #include "sv_internal.h"
 
 namespace sv {
 
-// Per (row, position) record in the workspace.
-struct SpecRec {
-    float ratio;  // p_k(x_k) / q_k(x_k) (sampling rows)
-    int flags;    // SPEC_* bits
-    int argmax;   // greedy rows: argmax of target row k
-    int token;    // sampling rows: the token drawn at k if k is the first rejection (bonus at k = K)
-};
+// The per-row word in the workspace: arrivals in bits [0, 11), reject bits of
+// positions 0..25 in [11, 37), invalid bits of positions 0..25 in [37, 63).  Every
+// CTA adds 1; rank 0 of position k's cluster also adds its two bits, each at most
+// once, so the fields never carry into each other.
+constexpr int SPEC_COUNT_BITS = 11;
+constexpr int SPEC_REJ_SHIFT = 11;
+constexpr int SPEC_BAD_SHIFT = 37;
+constexpr unsigned long long SPEC_FIELD_MASK = (1ull << SPEC_MAX_POS) - 1ull;
 
-constexpr int SPEC_BAD = 1;     // the position's rows (or q(x_k)) are invalid, or a staging wait gave up
-constexpr int SPEC_ACCEPT = 2;  // sampling: r_k < ratio; greedy: x_k == argmax
-
-// Workspace carve-up (256-byte aligned), identical on host and device: per-row arrival
-// counters, then per-(row, position) records.
 struct SpecWsLayout {
-    size_t counter_off, rec_off, total;
+    size_t counter_off, total;
 };
 
 __host__ __device__ inline size_t spec_align(size_t x) { return (x + 255) & ~(size_t)255; }
 
 __host__ __device__ inline SpecWsLayout spec_ws_layout(int B, int K) {
+    (void)K;
     SpecWsLayout L;
     L.counter_off = 0;
-    L.rec_off = spec_align((size_t)B * sizeof(unsigned));
-    L.total = spec_align(L.rec_off + (size_t)B * (K + 1) * sizeof(SpecRec));
+    L.total = spec_align((size_t)B * sizeof(unsigned long long));
     return L;
 }
 
@@ -59,50 +56,24 @@ struct SpecArgs {
     int d_bytes;  // bytes reserved for the draft chunk (tile sums follow)
 };
 
-// Finishing step for batch row b, run by the last CTA to arrive.
-__device__ __forceinline__ void spec_finish(const SpecArgs& A, int b, bool greedy, bool tok_bad, const int* s_tok,
-                                           SpecRec* s_rec, int* s_int) {
+// Finishing step for batch row b, run by the last CTA to arrive; `word` is the row's
+// final counter word (every position's bits are in it).
+__device__ __forceinline__ void spec_finish(const SpecArgs& A, int b, bool tok_bad, unsigned long long word) {
     const ChainArgs& a = A.a;
     const int K = a.K;
-    const SpecRec* grec = reinterpret_cast<const SpecRec*>(A.ws + A.wl.rec_off) + (size_t)b * (K + 1);
-    for (int i = threadIdx.x; i <= K; i += NT) {  // written by other SMs: read through L2
-        const int4 v = __ldcg(reinterpret_cast<const int4*>(&grec[i]));
-        s_rec[i] = SpecRec{__int_as_float(v.x), v.y, v.z, v.w};
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {  // first rejection (or mismatch): lowest k < K without SPEC_ACCEPT
-        int j = K;
-        for (int base = 0; base < K; base += 32) {
-            const int k = base + (int)threadIdx.x;
-            const unsigned rej = __ballot_sync(0xffffffffu, k < K && !(s_rec[k].flags & SPEC_ACCEPT));
-            if (rej) { j = base + __ffs(rej) - 1; break; }
-        }
-        int badb = 0;  // rows read up to and including j must be valid
-        for (int base = 0; base <= j; base += 32) {
-            const int k = base + (int)threadIdx.x;
-            if (__any_sync(0xffffffffu, k <= j && (s_rec[k].flags & SPEC_BAD))) badb = 1;
-        }
-        if (threadIdx.x == 0) {
-            s_int[1] = j;
-            s_int[2] = (tok_bad || badb) ? 1 : 0;
-        }
-    }
-    __syncthreads();
-    const int j = s_int[1];
-    const bool invalid = s_int[2] != 0;
-    const int final_tok = greedy ? s_rec[j].argmax : s_rec[j].token;
+    const unsigned long long rej = (word >> SPEC_REJ_SHIFT) & SPEC_FIELD_MASK;
+    const unsigned long long bad = (word >> SPEC_BAD_SHIFT) & SPEC_FIELD_MASK;
+    const int j = rej ? __ffsll((long long)rej) - 1 : K;  // first rejection, or K (every draft kept)
+    const bool invalid = tok_bad || (bad & ((2ull << j) - 1ull)) != 0ull;  // rows read up to j must be valid
     int32_t* ot = a.out_tokens + (size_t)b * (K + 1);
     for (int i = threadIdx.x; i <= K; i += NT)
-        ot[i] = invalid ? -1 : (i < j ? s_tok[i] : (i == j ? final_tok : -1));
+        if (invalid || i > j) ot[i] = -1;
     if (a.out_accept_prob)
-        for (int i = threadIdx.x; i < K; i += NT) {
-            float ap = -1.f;
-            if (!invalid && i <= j) ap = greedy ? ((s_rec[i].flags & SPEC_ACCEPT) ? 1.f : 0.f) : fminf(s_rec[i].ratio, 1.f);
-            a.out_accept_prob[(size_t)b * K + i] = ap;
-        }
+        for (int i = threadIdx.x; i < K; i += NT)
+            if (invalid || i > j) a.out_accept_prob[(size_t)b * K + i] = -1.f;
     if (threadIdx.x == 0) {
         a.out_count[b] = invalid ? 0 : j + 1;
-        *(reinterpret_cast<unsigned*>(A.ws + A.wl.counter_off) + b) = 0u;  // ready for the next call
+        *(reinterpret_cast<unsigned long long*>(A.ws + A.wl.counter_off) + b) = 0ull;  // ready for the next call
     }
 }
 
@@ -118,9 +89,9 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
     float* tile_sum = reinterpret_cast<float*>(db + A.d_bytes);  // the draw's tile sums
     __shared__ BlockScratch sc;
     __shared__ int s_tok[MAX_K];
-    __shared__ SpecRec s_rec[MAX_K + 1];
     __shared__ float s_flt[4];
-    __shared__ int s_int[4];
+    __shared__ unsigned long long s_word;  // the row's counter word after this CTA's atomic
+    __shared__ int s_last;
 
     const int G = (int)cluster_size(), g = (int)cluster_rank();
     const int k = blockIdx.y, b = blockIdx.z;
@@ -185,15 +156,16 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
     }
     const int fail = __syncthreads_or(!ok);
     const int x = (k < K && !tokens_bad) ? s_tok[k] : -1;
-    SpecRec* rec = reinterpret_cast<SpecRec*>(A.ws + A.wl.rec_off) + (size_t)b * (K + 1) + k;
-    int phase = 0, flags = 0, amax = -1;
+    int32_t* slot = a.out_tokens + (size_t)b * (K + 1) + k;  // this position's output slot
+    int phase = 0, amax = -1;
+    bool accept = false, bad = false;
     float ratio = 0.f;
     if (greedy) {
         ArgMax am = smem_thread_argmax<TDT>(tb, n, lo);
         if (fail) am.bad = 1;
         am = cluster_argmax(am, sc, phase);
-        if (am.bad || !(am.v > neg_inf()) || am.v == pos_inf()) flags |= SPEC_BAD;
-        if (k < K && x == am.i) flags |= SPEC_ACCEPT;
+        bad = am.bad || !(am.v > neg_inf()) || am.v == pos_inf();
+        accept = k < K && x == am.i;
         amax = am.i;
     } else {
         LSE ts = smem_thread_lse<TDT>(tb, n, c);
@@ -208,7 +180,7 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
             has = 1;
         }
         const PosStats ps = cluster_pos_stats<DK == DK_LOGITS>(ts, ds, c, tx, dx, has, sc, phase);
-        bool bad = row_bad_s(ps.t) || (DK == DK_LOGITS && k < K && row_bad_s(ps.d));
+        bad = row_bad_s(ps.t) || (DK == DK_LOGITS && k < K && row_bad_s(ps.d));
         const float inv_st = 1.f / ps.t.s;
         const float inv_sd = (DK == DK_LOGITS && k < K) ? 1.f / ps.d.s : 0.f;
         if (k < K && !bad) {
@@ -216,10 +188,11 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
             const float qx = (DK == DK_LOGITS) ? ex2((ps.dx - ps.d.m) * c) * inv_sd : ps.dx;
             if (DK == DK_PROBS && (!(qx >= 0.f) || qx == pos_inf())) bad = true;
             ratio = qx > 0.f ? px / qx : (px > 0.f ? pos_inf() : 0.f);
-            if (s_flt[0] < ratio) flags |= SPEC_ACCEPT;
+            accept = s_flt[0] < ratio;
         }
-        // 3. the draw at k, as if k were the first rejection (the bonus draw at k = K)
-        if (!bad && !tokens_bad) {
+        // 3. the draw at k, as if k were the first rejection (the bonus draw at k = K);
+        // a kept draft can never be the first rejection, so it needs no draw
+        if (!bad && !tokens_bad && !accept) {
             const float u = s_flt[1];
             DrawResult d;
             if (k < K) {
@@ -239,32 +212,40 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
                 d = cluster_draw(pw, lo, hi, u, tile_sum, sc, phase);
             }
             if (d.failed || d.owner < 0) bad = true;
-            else if (d.owner == g && threadIdx.x == 0) rec->token = d.token;
+            else if (d.owner == g && threadIdx.x == 0) *slot = d.token;
         }
-        if (bad) flags |= SPEC_BAD;
     }
     // a copy still in flight must land before the CTA exits (a greedy or invalid row
     // never waited for its q chunk)
     if (!draft_landed && threadIdx.x == 0) (void)mbar_wait_bounded(dbar, 0);
-    // 4. publish the position record and count this CTA in
-    if (g == 0 && threadIdx.x == 0) {
-        rec->ratio = ratio;
-        rec->flags = flags;
-        rec->argmax = amax;
+    // 4. output slot k (a kept draft, or the greedy row's argmax; a sampling row's draw
+    // was written by its owner CTA) and the acceptance probability, then count this CTA
+    // in with the position's reject and invalid bits
+    if (g == 0 && threadIdx.x == 0 && !bad && !tokens_bad) {
+        if (accept) *slot = x;
+        else if (greedy) *slot = amax;
+        if (k < K && a.out_accept_prob)
+            a.out_accept_prob[(size_t)b * K + k] = greedy ? (accept ? 1.f : 0.f) : fminf(ratio, 1.f);
     }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        unsigned* counter = reinterpret_cast<unsigned*>(A.ws + A.wl.counter_off) + b;
-        const unsigned old = atomicAdd(counter, 1u);
-        s_int[0] = (old == (unsigned)((K + 1) * G - 1)) ? 1 : 0;
+        unsigned long long inc = 1ull;
+        if (g == 0) {
+            if (k < K && !accept) inc |= 1ull << (SPEC_REJ_SHIFT + k);
+            if (bad) inc |= 1ull << (SPEC_BAD_SHIFT + k);
+        }
+        unsigned long long* word = reinterpret_cast<unsigned long long*>(A.ws + A.wl.counter_off) + b;
+        const unsigned long long old = atomicAdd(word, inc);
+        s_word = old + inc;
+        s_last = (old & ((1ull << SPEC_COUNT_BITS) - 1ull)) == (unsigned long long)((K + 1) * G - 1) ? 1 : 0;
     }
     __syncthreads();
-    const bool last = s_int[0] != 0;
+    const bool last = s_last != 0;
     cluster_sync_all();  // every remote shared-memory access of this cluster is done
     if (!last) return;
     __threadfence();
-    spec_finish(A, b, greedy, tokens_bad, s_tok, s_rec, s_int);
+    spec_finish(A, b, tokens_bad, s_word);
 }
 
 

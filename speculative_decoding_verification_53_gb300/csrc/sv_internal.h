@@ -48,6 +48,10 @@ struct SampleArgs {
     int32_t* out_draft_tokens; // [B][K]
 };
 
+// Positions (K + 1) the position-parallel chain kernel takes: its per-row counter word
+// carries a reject bit and an invalid bit per position.
+constexpr int SPEC_MAX_POS = 26;
+
 // Per-tree arrays of the staged tree kernel in dynamic shared memory (N nodes): tokens,
 // parents, children / depth counts, jump targets, accept uniforms (N each), draw
 // uniforms (N + 1) and the rejection history (tried token, applied flag: N each;

@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)2 << 20;  // 2 MiB, held by every device that loads the library
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)256 << 10;  // 256 KiB, held by every device that loads the library
 constexpr int NOALLOC_MAX_DEVICES = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
