@@ -12,10 +12,10 @@
 //      first rejection (the replacement from (p_k - q_k)+, or from p_k when that
 //      residual is empty; the bonus token from p_K at k = K), inside the cluster
 //      and from shared memory;
-//   3. it writes output slot k itself (x_k when accepted, else the drawn token)
-//      and counts itself in with one 64-bit atomic that also carries the
-//      position's reject and invalid bits.
-// The last CTA to arrive for batch row b (no CTA ever waits for another) reads
+//   3. one CTA of the cluster writes output slot k (x_k when accepted, else the
+//      drawn token) and counts the position in with one 64-bit atomic that also
+//      carries the position's reject and invalid bits.
+// The last position to arrive for batch row b (no CTA ever waits for another) reads
 // the first rejection j and the invalid bits off the value its own atomic
 // returned, clears the slots after j and writes the count.  The results are
 // those of the left-to-right rule; the price of the shorter critical path is that
@@ -26,9 +26,9 @@
 namespace sv {
 
 // The per-row word in the workspace: arrivals in bits [0, 11), reject bits of
-// positions 0..25 in [11, 37), invalid bits of positions 0..25 in [37, 63).  Every
-// CTA adds 1; rank 0 of position k's cluster also adds its two bits, each at most
-// once, so the fields never carry into each other.
+// positions 0..25 in [11, 37), invalid bits of positions 0..25 in [37, 63).  One CTA
+// of each position's cluster adds 1 plus the position's two bits, each at most once,
+// so the fields never carry into each other.
 constexpr int SPEC_COUNT_BITS = 11;
 constexpr int SPEC_REJ_SHIFT = 11;
 constexpr int SPEC_BAD_SHIFT = 37;
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
     const int fail = __syncthreads_or(!ok);
     const int x = (k < K && !tokens_bad) ? s_tok[k] : -1;
     int32_t* slot = a.out_tokens + (size_t)b * (K + 1) + k;  // this position's output slot
-    int phase = 0, amax = -1;
+    int phase = 0, amax = -1, owner = -1, token = -1;
     bool accept = false, bad = false;
     float ratio = 0.f;
     if (greedy) {
@@ -212,38 +212,39 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
                 d = cluster_draw(pw, lo, hi, u, tile_sum, sc, phase);
             }
             if (d.failed || d.owner < 0) bad = true;
-            else if (d.owner == g && threadIdx.x == 0) *slot = d.token;
+            owner = d.owner;
+            token = d.token;  // valid in the owner CTA
         }
     }
     // a copy still in flight must land before the CTA exits (a greedy or invalid row
     // never waited for its q chunk)
     if (!draft_landed && threadIdx.x == 0) (void)mbar_wait_bounded(dbar, 0);
-    // 4. output slot k (a kept draft, or the greedy row's argmax; a sampling row's draw
-    // was written by its owner CTA) and the acceptance probability, then count this CTA
-    // in with the position's reject and invalid bits
-    if (g == 0 && threadIdx.x == 0 && !bad && !tokens_bad) {
-        if (accept) *slot = x;
-        else if (greedy) *slot = amax;
-        if (k < K && a.out_accept_prob)
-            a.out_accept_prob[(size_t)b * K + k] = greedy ? (accept ? 1.f : 0.f) : fminf(ratio, 1.f);
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned long long inc = 1ull;
-        if (g == 0) {
-            if (k < K && !accept) inc |= 1ull << (SPEC_REJ_SHIFT + k);
-            if (bad) inc |= 1ull << (SPEC_BAD_SHIFT + k);
+    // 4. one CTA reports the position (all of them know its outcome): the owner of the
+    // drawn token when there is a draw, else rank 0.  It writes output slot k (the kept
+    // draft, the greedy row's argmax or the drawn token) and the acceptance probability,
+    // then counts the position in with its reject and invalid bits.
+    const bool drawn = !greedy && !bad && !tokens_bad && !accept;
+    const int reporter = drawn ? owner : 0;
+    if (g == reporter && threadIdx.x == 0) {
+        if (!bad && !tokens_bad) {
+            *slot = accept ? x : (greedy ? amax : token);
+            if (k < K && a.out_accept_prob)
+                a.out_accept_prob[(size_t)b * K + k] = greedy ? (accept ? 1.f : 0.f) : fminf(ratio, 1.f);
         }
+        __threadfence();
+        unsigned long long inc = 1ull;
+        if (k < K && !accept) inc |= 1ull << (SPEC_REJ_SHIFT + k);
+        if (bad) inc |= 1ull << (SPEC_BAD_SHIFT + k);
         unsigned long long* word = reinterpret_cast<unsigned long long*>(A.ws + A.wl.counter_off) + b;
         const unsigned long long old = atomicAdd(word, inc);
         s_word = old + inc;
-        s_last = (old & ((1ull << SPEC_COUNT_BITS) - 1ull)) == (unsigned long long)((K + 1) * G - 1) ? 1 : 0;
+        s_last = (old & ((1ull << SPEC_COUNT_BITS) - 1ull)) == (unsigned long long)K ? 1 : 0;  // K + 1 positions
     }
     __syncthreads();
-    const bool last = s_last != 0;
-    cluster_sync_all();  // every remote shared-memory access of this cluster is done
-    if (!last) return;
+    // Every cluster collective of this kernel pushes into the peers' shared memory before
+    // a cluster barrier and then reads only its own, so once the last collective's
+    // barrier is passed no CTA touches another's shared memory: CTAs may leave now.
+    if (g != reporter || s_last == 0) return;
     __threadfence();
     spec_finish(A, b, tokens_bad, s_word);
 }
