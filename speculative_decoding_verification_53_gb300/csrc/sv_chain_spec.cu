@@ -25,6 +25,15 @@
 
 namespace sv {
 
+// atomicAdd with acquire-release semantics at GPU scope: this thread's earlier global
+// writes are visible to whoever later reads the word's new value, and the writes of
+// every earlier adder are visible to this thread afterwards.
+__device__ __forceinline__ unsigned long long atomic_add_acq_rel(unsigned long long* p, unsigned long long v) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+
 // The per-row word in the workspace: arrivals in bits [0, 11), reject bits of
 // positions 0..25 in [11, 37), invalid bits of positions 0..25 in [37, 63).  One CTA
 // of each position's cluster adds 1 plus the position's two bits, each at most once,
@@ -231,12 +240,11 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
             if (k < K && a.out_accept_prob)
                 a.out_accept_prob[(size_t)b * K + k] = greedy ? (accept ? 1.f : 0.f) : fminf(ratio, 1.f);
         }
-        __threadfence();
         unsigned long long inc = 1ull;
         if (k < K && !accept) inc |= 1ull << (SPEC_REJ_SHIFT + k);
         if (bad) inc |= 1ull << (SPEC_BAD_SHIFT + k);
         unsigned long long* word = reinterpret_cast<unsigned long long*>(A.ws + A.wl.counter_off) + b;
-        const unsigned long long old = atomicAdd(word, inc);
+        const unsigned long long old = atomic_add_acq_rel(word, inc);  // releases the slot just written
         s_word = old + inc;
         s_last = (old & ((1ull << SPEC_COUNT_BITS) - 1ull)) == (unsigned long long)K ? 1 : 0;  // K + 1 positions
     }
@@ -245,7 +253,8 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
     // a cluster barrier and then reads only its own, so once the last collective's
     // barrier is passed no CTA touches another's shared memory: CTAs may leave now.
     if (g != reporter || s_last == 0) return;
-    __threadfence();
+    // thread 0's acquiring add made every position's slot writes visible to it; the
+    // barrier above carries that to the rest of the CTA
     spec_finish(A, b, tokens_bad, s_word);
 }
 
