@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(NT) chain_kernel(const ChainArgs a) {
     __shared__ BlockScratch sc;
     __shared__ int s_tok[MAX_K];
     __shared__ float s_r[MAX_K + 1], s_u[MAX_K + 1], s_ap[MAX_K];
+    xchg_init(sc);  // inbox barriers of the cluster exchanges (shared memory only)
 
     pdl_trigger();
     pdl_wait();  // nothing the previous kernel on the stream writes is read before this

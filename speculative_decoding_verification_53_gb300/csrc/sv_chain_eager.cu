@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(NT) chain_eager_kernel(const EagerArgs E) {
     __shared__ float2 gval[EAGER_MAX_POS];
     __shared__ int s_tok[EAGER_MAX_POS], s_res[4];
     __shared__ float s_r[EAGER_MAX_POS], s_u[EAGER_MAX_POS], s_qx[EAGER_MAX_POS], s_ap[EAGER_MAX_POS];
+    xchg_init(sc);  // inbox barriers of the cluster exchanges (shared memory only)
 
     const int G = (int)cluster_size(), g = (int)cluster_rank();
     const int b = blockIdx.y;

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
     __shared__ float s_flt[4];
     __shared__ unsigned long long s_word;  // the row's counter word after this CTA's atomic
     __shared__ int s_last;
+    xchg_init(sc);  // inbox barriers of the cluster exchanges (shared memory only)
 
     const int G = (int)cluster_size(), g = (int)cluster_rank();
     const int k = blockIdx.y, b = blockIdx.z;

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     __shared__ int s_tok[MAX_K];
     __shared__ float s_r[MAX_K + 1], s_u[MAX_K + 1], s_ap[MAX_K];
     __shared__ float s_qx;
+    xchg_init(sc);  // inbox barriers of the cluster exchanges (shared memory only)
 
     const int G = (int)cluster_size(), g = (int)cluster_rank();
     const int b = blockIdx.y;

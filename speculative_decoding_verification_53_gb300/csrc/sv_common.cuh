@@ -314,6 +314,87 @@ __device__ __forceinline__ uint32_t cluster_size() {
 
 // Every thread of every CTA of the cluster arrives and waits (release/acquire on
 // shared::cluster), so DSMEM writes before it are visible after it.
+// ------------------------------------------------------------- mbarriers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async proxy (the bulk-copy engine).
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+// Order this CTA's generic-proxy accesses of shared memory before later async-proxy writes.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Raise the expected transaction bytes of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// try_wait with a suspend-time hint: the thread may be suspended in hardware (woken when
+// the phase completes) for up to `ns` nanoseconds instead of returning at once, so a
+// waiting warp does not spin through issue slots other warps could use.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete.  Gives up and returns false
+// after a quarter of a second (global timer) or 2^22 tries, whichever comes first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
+        if (global_ns() - t0 > 250000000ull) break;
+    }
+    return false;
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -338,11 +419,29 @@ __device__ __forceinline__ void dsmem_st_v2(uint32_t addr, float2 v) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
 }
 
+// Store into a peer CTA's shared memory whose bytes complete a transaction count on
+// that CTA's mbarrier `mbar` (a shared::cluster address): the receiver learns from its
+// own barrier that the data has landed, with no cluster-wide barrier.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(mbar)
+                 : "memory");
+}
 
-// Inbox of pushed partials: every warp of every CTA of the cluster stores its
-// (target max, target sum, draft max, draft sum) here with a remote store, so after
-// one cluster barrier the combine reads local shared memory only.  A NaN sum marks a
-// row that contained NaN.  Double-buffered by exchange phase.
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float2 v, uint32_t mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "f"(v.x), "f"(v.y), "r"(mbar)
+                 : "memory");
+}
+
+
+// Inbox of pushed partials.  In an exchange every CTA of the cluster stores its
+// partials into every CTA's inbox (its own included) with st.async, each store
+// completing its bytes on the receiver's barrier of that buffer; a CTA waits on its
+// own barrier only, then combines from local shared memory.  A NaN sum marks a row
+// that contained NaN.  Double-buffered by exchange number: a CTA sends exchange e+1
+// only after it has read exchange e, so a buffer is never overwritten while read.
 struct Inbox {
     float4 part[2][MAX_CLUSTER][NW];
     float4 gath[2][MAX_CLUSTER];  // (target value, draft value, has, -) at the drafted token
@@ -351,6 +450,7 @@ struct Inbox {
 
 // Shared state of a CTA used by the block- and cluster-level reductions.
 struct BlockScratch {
+    uint64_t xbar[2];  // one mbarrier per inbox buffer
     Inbox inbox;
     float rf[NW][4];
     int ri[NW][2];
@@ -367,13 +467,42 @@ __device__ __forceinline__ void chunk_range(int V, int g, int G, int& lo, int& h
     if (lo > V) lo = V;
 }
 
+// Sets up the inbox barriers; every thread of every CTA of the cluster calls it once,
+// before the first exchange.  Its cluster barrier makes every CTA's barriers exist
+// before any peer sends.  No global memory is touched (it may precede pdl_wait).
+__device__ __forceinline__ void xchg_init(BlockScratch& sc) {
+    if (threadIdx.x == 0) {
+        mbar_init(&sc.xbar[0], 1);
+        mbar_init(&sc.xbar[1], 1);
+        fence_mbar_init();
+    }
+    cluster_sync_all();
+}
+
+// Exchange number `phase` uses inbox buffer phase & 1, whose barrier completes its
+// (phase >> 1)-th phase.  Thread 0 arms it with the bytes all G senders will deliver.
+__device__ __forceinline__ void xchg_arm(BlockScratch& sc, int phase, uint32_t bytes) {
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&sc.xbar[phase & 1], bytes);
+}
+
+// The receiver's barrier of this exchange, in CTA `peer`'s window.
+__device__ __forceinline__ uint32_t xchg_bar(BlockScratch& sc, int phase, uint32_t peer) {
+    return dsmem_addr(&sc.xbar[phase & 1], peer);
+}
+
+// Bounded wait for this CTA's inbox of exchange `phase` to be complete.
+__device__ __forceinline__ bool xchg_wait(BlockScratch& sc, int phase) {
+    return mbar_wait_bounded(&sc.xbar[phase & 1], (uint32_t)(phase >> 1) & 1u);
+}
+
 // Block reduce of up to two LSE pairs, then a cluster-wide combine in rank order.
-// Every thread of every CTA returns the same values.  Push model: warp 0 stores the
-// CTA's pairs into every peer's inbox, one cluster barrier, then a local combine.
+// Every thread of every CTA returns the same values.  Warp 0 sends the CTA's pairs
+// into every inbox, then waits for its own and combines locally.
 __device__ __forceinline__ void cluster_lse2(LSE& a, LSE& b, float c, BlockScratch& sc, int& phase) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t G = cluster_size(), me = cluster_rank();
     const int buf = phase & 1;
+    xchg_arm(sc, phase, G * 32u);
     lse_warp_reduce(a, c);
     lse_warp_reduce(b, c);
     if (lane == 0) {
@@ -391,19 +520,19 @@ __device__ __forceinline__ void cluster_lse2(LSE& a, LSE& b, float c, BlockScrat
         lse_warp_reduce(x, c);
         lse_warp_reduce(y, c);
         if ((uint32_t)lane < G) {
-            const uint32_t peer = (uint32_t)lane;
-            dsmem_st_v4(dsmem_addr(&sc.inbox.part[buf][me][0], peer), make_float4(x.m, x.s, y.m, y.s));
-            dsmem_st_v4(dsmem_addr(&sc.inbox.part[buf][me][1], peer),
-                        make_float4(__int_as_float(x.bad), __int_as_float(y.bad), 0.f, 0.f));
+            const uint32_t peer = (uint32_t)lane, bar = xchg_bar(sc, phase, peer);
+            st_async_v4(dsmem_addr(&sc.inbox.part[buf][me][0], peer), make_float4(x.m, x.s, y.m, y.s), bar);
+            st_async_v4(dsmem_addr(&sc.inbox.part[buf][me][1], peer),
+                        make_float4(__int_as_float(x.bad), __int_as_float(y.bad), 0.f, 0.f), bar);
         }
     }
-    cluster_sync_all();
     if (warp == 0) {
+        const int ok = __all_sync(0xffffffffu, xchg_wait(sc, phase)) ? 1 : 0;
         LSE x{neg_inf(), 0.f, 0}, y{neg_inf(), 0.f, 0};
         if ((uint32_t)lane < G) {
             const float4 v = sc.inbox.part[buf][lane][0], f = sc.inbox.part[buf][lane][1];
-            x = LSE{v.x, v.y, __float_as_int(f.x)};
-            y = LSE{v.z, v.w, __float_as_int(f.y)};
+            x = LSE{v.x, v.y, __float_as_int(f.x) | (ok ? 0 : 1)};
+            y = LSE{v.z, v.w, __float_as_int(f.y) | (ok ? 0 : 1)};
         }
         lse_warp_reduce(x, c);
         lse_warp_reduce(y, c);
@@ -420,18 +549,19 @@ __device__ __forceinline__ void cluster_lse2(LSE& a, LSE& b, float c, BlockScrat
 }
 
 __device__ __forceinline__ ArgMax cluster_argmax(ArgMax a, BlockScratch& sc, int& phase) {
-    // Push model (as the statistics combine): lanes 0..G-1 of every warp store the warp's
-    // (max, index, NaN flag) into CTA `lane`'s inbox, then each CTA reduces locally.
+    // Lanes 0..G-1 of every warp send the warp's (max, index, NaN flag) into CTA
+    // `lane`'s inbox; each CTA waits for its own inbox and reduces locally.
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = (int)cluster_size(), me = (int)cluster_rank();
     const int buf = phase & 1;
+    xchg_arm(sc, phase, (uint32_t)(G * NW) * 16u);
     argmax_warp_reduce(a);
     if (lane < G)
-        dsmem_st_v4(dsmem_addr(&sc.inbox.part[buf][me][warp], (uint32_t)lane),
-                    make_float4(a.v, __int_as_float(a.i), __int_as_float(a.bad), 0.f));
-    cluster_sync_all();
+        st_async_v4(dsmem_addr(&sc.inbox.part[buf][me][warp], (uint32_t)lane),
+                    make_float4(a.v, __int_as_float(a.i), __int_as_float(a.bad), 0.f), xchg_bar(sc, phase, lane));
     if (warp == 0) {
-        ArgMax x{neg_inf(), 0x7fffffff, 0};
+        const bool ok = __all_sync(0xffffffffu, xchg_wait(sc, phase));
+        ArgMax x{neg_inf(), 0x7fffffff, ok ? 0 : 1};
         for (int e = lane; e < G * NW; e += 32) {
             const float4 v = sc.inbox.part[buf][e / NW][e % NW];
             argmax_merge(x, ArgMax{v.x, __float_as_int(v.y), __float_as_int(v.z)});
@@ -450,13 +580,14 @@ __device__ __forceinline__ ArgMax cluster_argmax(ArgMax a, BlockScratch& sc, int
     return r;
 }
 
-// Cluster-wide sum of two floats (fixed order, identical in every CTA).  Push model:
-// warp 0 stores the CTA's pair into every peer's inbox, one cluster barrier, then
-// each CTA adds its own inbox in rank order.
+// Cluster-wide sum of two floats (fixed order, identical in every CTA).  Warp 0 sends
+// the CTA's pair into every inbox, waits for its own and adds it in rank order.  A
+// wait that gives up returns NaN sums.
 __device__ __forceinline__ float2 cluster_sum2(float2 v, BlockScratch& sc, int& phase) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t G = cluster_size(), me = cluster_rank();
     const int buf = phase & 1;
+    xchg_arm(sc, phase, G * 8u);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
@@ -472,12 +603,13 @@ __device__ __forceinline__ float2 cluster_sum2(float2 v, BlockScratch& sc, int& 
             x.x += __shfl_xor_sync(0xffffffffu, x.x, o);
             x.y += __shfl_xor_sync(0xffffffffu, x.y, o);
         }
-        if ((uint32_t)lane < G) dsmem_st_v2(dsmem_addr(&sc.inbox.zf[buf][me], (uint32_t)lane), x);
+        if ((uint32_t)lane < G)
+            st_async_v2(dsmem_addr(&sc.inbox.zf[buf][me], (uint32_t)lane), x, xchg_bar(sc, phase, (uint32_t)lane));
     }
-    cluster_sync_all();
     if (warp == 0) {
+        const bool ok = __all_sync(0xffffffffu, xchg_wait(sc, phase));
         float2 x = make_float2(0.f, 0.f);
-        if ((uint32_t)lane < G) x = sc.inbox.zf[buf][lane];
+        if ((uint32_t)lane < G) x = ok ? sc.inbox.zf[buf][lane] : make_float2(nanf(""), nanf(""));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             x.x += __shfl_xor_sync(0xffffffffu, x.x, o);
@@ -521,24 +653,26 @@ __device__ __forceinline__ DrawResult cluster_draw_from_tiles(const WF& wf, int 
                                               BlockScratch& sc, int& phase, int fail_in = 0) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ntiles = (hi - lo + TILE - 1) / TILE;
+    xchg_arm(sc, phase, cluster_size() * 8u);
     if (warp == 0) {
         float z = 0.f;
         for (int t = lane; t < ntiles; t += 32) z += tile_sum[t];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         const uint32_t Gp = cluster_size(), me = cluster_rank();
-        if ((uint32_t)lane < Gp)  // push (total, failure) into every peer's inbox
-            dsmem_st_v2(dsmem_addr(&sc.inbox.zf[phase & 1][me], (uint32_t)lane), make_float2(z, (float)fail_in));
+        if ((uint32_t)lane < Gp)  // send (total, failure) into every inbox
+            st_async_v2(dsmem_addr(&sc.inbox.zf[phase & 1][me], (uint32_t)lane), make_float2(z, (float)fail_in),
+                        xchg_bar(sc, phase, (uint32_t)lane));
     }
-    cluster_sync_all();
     if (warp == 0) {
         const uint32_t G = cluster_size();
+        const bool ok = __all_sync(0xffffffffu, xchg_wait(sc, phase));
         float z = 0.f;
-        int fl = 0;
+        int fl = ok ? 0 : 1;
         if ((uint32_t)lane < G) {
             const float2 v = sc.inbox.zf[phase & 1][lane];
             z = v.x;
-            fl = v.y != 0.f ? 1 : 0;
+            fl |= v.y != 0.f ? 1 : 0;
         }
         const int any_fail = __any_sync(0xffffffffu, fl != 0) ? 1 : 0;
         float incl = z;

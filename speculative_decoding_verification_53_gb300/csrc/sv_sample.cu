@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(const SampleArgs a) {
     pdl_wait();  // nothing the previous kernel on the stream writes is read before this
     extern __shared__ float tile_sum[];
     __shared__ BlockScratch sc;
+    xchg_init(sc);  // inbox barriers of the cluster exchanges (shared memory only)
     const int g = (int)cluster_rank(), G = (int)cluster_size();
     const int k = (int)blockIdx.y, b = (int)blockIdx.z;
     const int V = a.V;
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(NT) draft_sample_staged_kernel(const SampleArg
     float* tile_sum = reinterpret_cast<float*>(db + chunk_bytes);
     __shared__ BlockScratch sc;
     __shared__ float s_u;
+    xchg_init(sc);  // inbox barriers of the cluster exchanges (shared memory only)
     const int g = (int)cluster_rank(), G = (int)cluster_size();
     const int k = (int)blockIdx.y, b = (int)blockIdx.z;
     const int V = a.V;

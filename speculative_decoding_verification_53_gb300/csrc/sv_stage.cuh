@@ -14,85 +14,6 @@
 
 namespace sv {
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-// Make barrier initialisation visible to the async proxy (the bulk-copy engine).
-__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-
-// Order this CTA's generic-proxy accesses of shared memory before later async-proxy writes.
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-// Raise the expected transaction bytes of the current phase without arriving.
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// try_wait with a suspend-time hint: the thread may be suspended in hardware (woken when
-// the phase completes) for up to `ns` nanoseconds instead of returning at once, so a
-// waiting warp does not spin through issue slots other warps could use.
-__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the phase with the given parity to complete.  Gives up and returns false
-// after a quarter of a second (global timer) or 2^22 tries, whichever comes first.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 0; i < (1u << 22); ++i) {
-        if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
-        if (global_ns() - t0 > 250000000ull) break;
-    }
-    return false;
-}
-
 // Elements per 16-byte smem vector step: 8 values (bf16: one 16 B read; fp32: two).
 template <int DT>
 __device__ __forceinline__ void smem_load8(const unsigned char* buf, int e, int n, float pad, float x[VEC]) {
@@ -220,14 +141,15 @@ struct PosStats {
 template <bool TWO>
 __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, float tx, float dx, int has,
                                                       BlockScratch& sc, int& phase) {
-    // Push model: lanes 0..G-1 of every warp store the warp's partials into CTA
-    // `lane`'s inbox; thread 0 also pushes the values it gathered at x_k.  One
-    // cluster barrier later each CTA combines its own inbox from local memory:
-    // every lane takes up to four partials, then a warp maximum, one rescale per
-    // partial and a warp sum.
+    // Lanes 0..G-1 of every warp send the warp's partials into CTA `lane`'s inbox;
+    // warp 0 also sends the values thread 0 gathered at x_k.  Each CTA waits for its
+    // own inbox (its barrier counts the bytes) and combines from local memory: every
+    // lane takes up to four partials, then a warp maximum, one rescale per partial and
+    // a warp sum.
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = (int)cluster_size(), me = (int)cluster_rank();
     const int buf = phase & 1;
+    xchg_arm(sc, phase, (uint32_t)(G * (NW + 1)) * 16u);
     if (TWO) {
         lse2_warp_reduce(t, d, c);
     } else {
@@ -236,16 +158,17 @@ __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, flo
     if (lane < G) {
         const float4 v = make_float4(t.m, t.bad ? __int_as_float(0x7fffffff) : t.s, TWO ? d.m : neg_inf(),
                                      (TWO && d.bad) ? __int_as_float(0x7fffffff) : (TWO ? d.s : 0.f));
-        dsmem_st_v4(dsmem_addr(&sc.inbox.part[buf][me][warp], (uint32_t)lane), v);
+        st_async_v4(dsmem_addr(&sc.inbox.part[buf][me][warp], (uint32_t)lane), v, xchg_bar(sc, phase, lane));
     }
     if (warp == 0) {
         const float gtx = __shfl_sync(0xffffffffu, tx, 0), gdx = __shfl_sync(0xffffffffu, dx, 0);
         const int ghas = __shfl_sync(0xffffffffu, has, 0);
         if (lane < G)
-            dsmem_st_v4(dsmem_addr(&sc.inbox.gath[buf][me], (uint32_t)lane), make_float4(gtx, gdx, (float)ghas, 0.f));
+            st_async_v4(dsmem_addr(&sc.inbox.gath[buf][me], (uint32_t)lane), make_float4(gtx, gdx, (float)ghas, 0.f),
+                        xchg_bar(sc, phase, lane));
     }
-    cluster_sync_all();
     if (warp == 0) {
+        const bool ok = __all_sync(0xffffffffu, xchg_wait(sc, phase));
         const int E = G * NW;  // at most 16 * 8 = 128 partials: four per lane
         float4 v[4];
 #pragma unroll
@@ -278,7 +201,7 @@ __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, flo
             St += __shfl_xor_sync(0xffffffffu, St, o);
             if (TWO) Sd += __shfl_xor_sync(0xffffffffu, Sd, o);
         }
-        bt = __any_sync(0xffffffffu, bt) ? 1 : 0;
+        bt = (__any_sync(0xffffffffu, bt) || !ok) ? 1 : 0;  // a wait that gave up voids the row
         bd = __any_sync(0xffffffffu, bd) ? 1 : 0;
         float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
         if (lane < G) gv = sc.inbox.gath[buf][lane];

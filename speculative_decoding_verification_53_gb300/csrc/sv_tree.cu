@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(NT) tree_kernel(const TreeArgs a) {
     __shared__ int s_out[65], s_path[64];
     __shared__ int s_nchild, s_flag;
     __shared__ TreeHistory hs;
+    xchg_init(sc);  // inbox barriers of the cluster exchanges (shared memory only)
 
     const int G = (int)cluster_size(), g = (int)cluster_rank();
     const int b = blockIdx.y;

@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
     __shared__ float s_rt[TREE_GATHER], s_rd[TREE_GATHER];
     __shared__ int s_out[65], s_path[64];
     __shared__ int s_nchild, s_hn;
+    xchg_init(sc);  // inbox barriers of the cluster exchanges (shared memory only)
 
     const int G = (int)cluster_size(), g = (int)cluster_rank();
     const int b = blockIdx.y;
