@@ -23,6 +23,11 @@ def main():
         excused += compare(gpu_chain(ws, seed=s, offset=s), oracle_chain(ws, seed=s, offset=s))
     w = synth.large_batch(seed=4, temperature=1.0, sigma=1.0, B=3, K=8)
     excused += compare(gpu_chain(w, seed=9), oracle_chain(w, seed=9))
+    from test_gpu_parity import _bad_after_first_rejection  # noqa: E402
+    w = _bad_after_first_rejection()
+    g = gpu_chain(w)
+    assert (g["count"] == 1).all(), g["count"]
+    excused += compare(g, oracle_chain(w))
     w = synth.tiny_chain(seed=8, V=4096, K=0, B=2)
     excused += compare(gpu_chain(w), oracle_chain(w))
     w = synth.tiny_chain(seed=9, V=1024, K=64, B=1, sigma=0.1)

@@ -207,6 +207,32 @@ def test_masked_invalid_and_zero_q_rows():
     assert (g["count"] == 4).all()
 
 
+def _bad_after_first_rejection():
+    """Rows whose first draft is surely rejected (p(x_0) = 0, or x_0 != argmax on greedy
+    rows) carry invalid data only at later positions, which the rule never reads."""
+    w = synth.tiny_chain(seed=6, V=640, K=4, B=6)
+    t, d, toks = w["target"].copy(), w["draft"].copy(), w["tokens"].copy()
+    temp = w["temperature"].copy()
+    for b in range(6):
+        t[b, 0, toks[b, 0]] = -np.inf          # p_0(x_0) = 0: rejected at position 0
+    t[0, 2, 7] = np.nan
+    t[1, 3, :] = -np.inf
+    t[2, 4, 9] = np.inf
+    d[3, 2, 11] = np.nan                       # draft logits invalid at position 2
+    temp[4:] = 0.0                             # greedy rows: x_0 is not the argmax (its logit is -inf)
+    t[4, 1, 3] = np.nan
+    t[5, 4, :] = -np.inf
+    return dict(w, target=t, draft=d, tokens=toks, temperature=temp)
+
+
+def test_invalid_rows_after_the_first_rejection_are_ignored():
+    w = _bad_after_first_rejection()
+    g, o = gpu_chain(w), oracle_chain(w)
+    assert (o["count"] == 1).all()
+    assert compare(g, o) == 0
+    assert (g["count"] == 1).all()
+
+
 def test_empty_batch_is_a_noop():
     import torch
     import speculative_decoding_verification_53_gb300 as sv
