@@ -573,19 +573,28 @@ def run_aux(args, rank, world, device):
     stream = torch.cuda.Stream(device)
     torch.cuda.set_stream(stream)
     chunk = min(args.steps, 1000)
+    n_graphs = 1
     if args.workload == "tree_mask":
-        dpar = torch.from_numpy(a["parent"]).to(device)
-        outs = [(torch.empty((a["B"], a["N"], a["W"]), dtype=torch.int32, device=device),
-                 torch.empty((a["B"], a["N"]), dtype=torch.int32, device=device),
-                 torch.empty((a["B"],), dtype=torch.int32, device=device)) for _ in range(2)]
+        # Distinct parent and output buffers per step, cycled, so that the bytes touched
+        # between two uses of one buffer exceed twice the L2.
+        l2_bytes = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (129 << 20)
+        n_sets = max(2, -(-2 * l2_bytes // a["bytes_per_step"]))
+        if n_sets > chunk:
+            n_graphs = -(-n_sets // chunk)
+            n_sets = n_graphs * chunk
+        dpar = torch.from_numpy(a["parent"]).to(device).unsqueeze(0).repeat(n_sets, 1, 1)
+        om = torch.empty((n_sets, a["B"], a["N"], a["W"]), dtype=torch.int32, device=device)
+        od = torch.empty((n_sets, a["B"], a["N"]), dtype=torch.int32, device=device)
+        ov = torch.empty((n_sets, a["B"]), dtype=torch.int32, device=device)
 
         def step(i):
-            m, d, v = outs[i % 2]
-            sv.spec_tree_mask(dpar, out_mask=m, out_depth=d, out_valid=v)
+            s = i % n_sets
+            sv.spec_tree_mask(dpar[s], out_mask=om[s], out_depth=od[s], out_valid=ov[s])
 
         def bytes_of(i):
             return a["bytes_per_step"]
-        l2 = "outputs of two alternating steps (2 x %.0f MB) larger than L2" % (a["B"] * a["N"] * a["W"] * 4 / 1e6)
+        l2 = "%d distinct parent/output sets cycled (%.0f MB between reuses, larger than L2)" % (
+            n_sets, n_sets * a["bytes_per_step"] / 1e6)
         kernel = "tree_mask_kernel"
     else:
         L = a["layout"]
@@ -614,12 +623,13 @@ def run_aux(args, rank, world, device):
     torch.cuda.synchronize(device)
     reps, rem = divmod(args.steps, chunk)
     graphs = []
-    for n in ([chunk] if reps else []) + ([rem] if rem else []):
+    for j, n in enumerate([chunk] * (min(reps, n_graphs) if reps else 0) + ([rem] if rem else [])):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                step(i)
+                step(j * chunk + i)
         graphs.append((g, n))
+    full = graphs[:min(reps, n_graphs)] if reps else []
     for g, _ in graphs:
         g.replay()
     torch.cuda.synchronize(device)
@@ -630,8 +640,8 @@ def run_aux(args, rank, world, device):
             torch.distributed.barrier()
         torch.cuda.synchronize(device)
         start.record(stream)
-        for _ in range(reps):
-            graphs[0][0].replay()
+        for r in range(reps):
+            full[r % len(full)][0].replay()
         if rem:
             graphs[-1][0].replay()
         end.record(stream)

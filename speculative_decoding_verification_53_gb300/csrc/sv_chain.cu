@@ -157,7 +157,9 @@ __global__ void __launch_bounds__(NT) chain_kernel(const ChainArgs a) {
             for (int i = threadIdx.x; i < K; i += NT) a.out_accept_prob[(size_t)b * K + i] = invalid ? -1.f : s_ap[i];
         if (threadIdx.x == 0) a.out_count[b] = invalid ? 0 : j + 1;
     }
-    cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+    // No trailing cluster barrier: peers only ever push into this CTA's inbox, and the
+    // last exchange (the same sequence in every CTA of the cluster) completed on this
+    // CTA's own barrier, so nothing is written into its shared memory any more.
 }
 
 size_t draw_smem_bytes(int V, int cluster) {

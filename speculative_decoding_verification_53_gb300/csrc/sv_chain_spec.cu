@@ -250,9 +250,9 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
         s_last = (old & ((1ull << SPEC_COUNT_BITS) - 1ull)) == (unsigned long long)K ? 1 : 0;  // K + 1 positions
     }
     __syncthreads();
-    // Every cluster collective of this kernel pushes into the peers' shared memory before
-    // a cluster barrier and then reads only its own, so once the last collective's
-    // barrier is passed no CTA touches another's shared memory: CTAs may leave now.
+    // Peers only ever push into this CTA's inbox, and the last exchange of the position
+    // (the same sequence in every CTA of the cluster) completed on this CTA's own
+    // barrier, so nothing is written into its shared memory any more: CTAs may leave now.
     if (g != reporter || s_last == 0) return;
     // thread 0's acquiring add made every position's slot writes visible to it; the
     // barrier above carries that to the rest of the CTA

@@ -31,8 +31,6 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     __shared__ int s_tok[MAX_K];
     __shared__ float s_r[MAX_K + 1], s_u[MAX_K + 1], s_ap[MAX_K];
     __shared__ float s_qx;
-    xchg_init(sc);  // inbox barriers of the cluster exchanges (shared memory only)
-
     const int G = (int)cluster_size(), g = (int)cluster_rank();
     const int b = blockIdx.y;
     const int K = a.K, V = a.V;
@@ -44,8 +42,6 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     const unsigned char* dbase = reinterpret_cast<const unsigned char*>(a.draft) + (size_t)b * K * V * dsz;
     const int first = (K + 1 < L.nslot) ? K + 1 : L.nslot;  // positions staged up front
 
-    // The target chunks of the first positions are requested before anything else, so
-    // their HBM latency overlaps the temperature, token and Philox work below.
     auto issue_t = [&](int k) {
         const int s = k % L.nslot;
         fence_proxy_async();
@@ -59,19 +55,29 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
             bulk_g2s(slots + (size_t)s * L.slot_bytes + L.t_bytes, dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz,
                      &dbar[s]);
     };
-    // the Philox blocks (kernel parameters only) on warps 1.. before the dependency wait;
-    // greedy rows simply never use them
-    for (int k = (int)threadIdx.x - 32; k >= 0 && k <= K; k += NT - 32)
-        slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, s_r[k], s_u[k]);
     if (threadIdx.x == 0) {
         for (int i = 0; i <= 2 * L.nslot; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
     }
+    // the Philox blocks (kernel parameters only) on warps 1.., before the dependency wait
+    // and off warp 0's path to the first copies; greedy rows simply never use them
+    for (int k = (int)threadIdx.x - 32; k >= 0 && k <= K; k += NT - 32)
+        slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, s_r[k], s_u[k]);
+    // inbox barriers of the cluster exchanges: set up and arrive now (no global memory
+    // is touched), wait in xchg_ready() just before the first exchange
+    xchg_init_arrive(sc);
     pdl_trigger();
     pdl_wait();  // nothing the previous kernel on the stream writes is read before this
+    // Start-up, shortest path to the first chunks first: the temperature and the tokens
+    // are requested ahead of the bulk copies (so they do not queue behind them), the
+    // target chunks go out at once, the draft-logit chunks as soon as the temperature
+    // says the row samples.  The wait at the cluster barrier that makes every CTA's
+    // exchange barriers exist and the token checks overlap the copies.
+    const float T = a.temperature ? a.temperature[b] : 0.f;
+    static_assert(NT >= MAX_K, "one drafted token per thread");
+    const int tok_reg = (int)threadIdx.x < K ? a.tokens[(size_t)b * K + threadIdx.x] : 0;
     if (threadIdx.x == 0)
         for (int k = 0; k < first; ++k) issue_t(k);
-    const float T = a.temperature ? a.temperature[b] : 0.f;
     const bool greedy = !(T > 0.f);
     const float c = greedy ? 0.f : LOG2E / T;
     const bool draft_rows = !greedy && DK == DK_LOGITS;  // draft-logit rows travel with the target rows
@@ -88,13 +94,13 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     }
 
     int tok_bad = 0;
-    for (int k = threadIdx.x; k < K; k += NT) {
-        const int x = a.tokens[(size_t)b * K + k];
-        s_tok[k] = x;
-        s_ap[k] = -1.f;
-        if (x < 0 || x >= V) tok_bad = 1;
+    if ((int)threadIdx.x < K) {
+        s_tok[threadIdx.x] = tok_reg;
+        s_ap[threadIdx.x] = -1.f;
+        if (tok_reg < 0 || tok_reg >= V) tok_bad = 1;
     }
     bool invalid = __syncthreads_or(tok_bad) != 0;
+    xchg_ready();
 
     auto issue = [&](int k) {  // refill: position k into slot k % nslot (its previous reads are done)
         const int s = k % L.nslot;
@@ -232,7 +238,9 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
                 a.out_accept_prob[(size_t)b * K + i] = invalid ? -1.f : s_ap[i];
         if (threadIdx.x == 0) a.out_count[b] = invalid ? 0 : j + 1;
     }
-    cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+    // No trailing cluster barrier: peers only ever push into this CTA's inbox, and the
+    // last exchange of the (cluster-uniform) walk completed on this CTA's own barrier,
+    // so nothing is written into its shared memory once it gets here.
 }
 
 size_t staged_smem_bytes(const StageLayout& L, int V, int G) {

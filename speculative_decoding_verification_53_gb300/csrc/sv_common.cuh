@@ -479,6 +479,24 @@ __device__ __forceinline__ void xchg_init(BlockScratch& sc) {
     cluster_sync_all();
 }
 
+// xchg_init split in two so that independent start-up work (issuing the first copies,
+// loading the tokens, the Philox blocks) overlaps the cluster barrier: xchg_init_arrive
+// sets up this CTA's inbox barriers and arrives; xchg_ready waits for every CTA's
+// arrival and must come before the first exchange.  Every thread calls each once, in
+// that order, with no other cluster barrier between them.
+__device__ __forceinline__ void xchg_init_arrive(BlockScratch& sc) {
+    if (threadIdx.x == 0) {
+        mbar_init(&sc.xbar[0], 1);
+        mbar_init(&sc.xbar[1], 1);
+        fence_mbar_init();
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void xchg_ready() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Exchange number `phase` uses inbox buffer phase & 1, whose barrier completes its
 // (phase >> 1)-th phase.  Thread 0 arms it with the bytes all G senders will deliver.
 __device__ __forceinline__ void xchg_arm(BlockScratch& sc, int phase, uint32_t bytes) {

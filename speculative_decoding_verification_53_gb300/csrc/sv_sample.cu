@@ -75,7 +75,9 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(const SampleArgs a) {
             }
         }
     }
-    cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+    // No trailing cluster barrier: peers only ever push into this CTA's inbox, and the
+    // last exchange (the same sequence in every CTA of the cluster) completed on this
+    // CTA's own barrier, so nothing is written into its shared memory any more.
 }
 
 template <int DDT>
@@ -135,7 +137,9 @@ __global__ void __launch_bounds__(NT) draft_sample_staged_kernel(const SampleArg
             }
         }
     }
-    cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+    // No trailing cluster barrier: peers only ever push into this CTA's inbox, and the
+    // last exchange (the same sequence in every CTA of the cluster) completed on this
+    // CTA's own barrier, so nothing is written into its shared memory any more.
 }
 
 // Cluster size: the largest power of two (at most 16, at least 2048 entries a CTA)

@@ -425,7 +425,9 @@ __global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const
         for (int i = threadIdx.x; i < D; i += NT) op[i] = (!invalid && i < emitted - 1) ? s_path[i] : -1;
         if (threadIdx.x == 0) a.out_count[b] = invalid ? 0 : emitted;
     }
-    cluster_sync_all();
+    // No trailing cluster barrier: peers only ever push into this CTA's inbox, and the
+    // last exchange (the same sequence in every CTA of the cluster) completed on this
+    // CTA's own barrier, so nothing is written into its shared memory any more.
 }
 
 
