@@ -211,14 +211,16 @@ __global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
                     dfail = __syncthreads_or(!mbar_wait_bounded(dbar, 0));
                     draft_landed = true;
                 }
-                const StagedResidual<TDT, DDT, DK> rw{tb, db, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd};
+                // one CTA per SM here: four tiles in flight per warp shorten the draw's
+                // dependent chains (the exp2 pipe has room)
+                const InFlight<StagedResidual<TDT, DDT, DK>, 4> rw{{tb, db, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd}};
                 d = cluster_draw(rw, lo, hi, u, tile_sum, sc, phase, dfail);
                 if (!d.failed && d.owner < 0) {  // the residual has no mass: draw from p_k
-                    const StagedP<TDT> pw{tb, lo, c, ps.t.m, inv_st};
+                    const InFlight<StagedP<TDT>, 4> pw{{tb, lo, c, ps.t.m, inv_st}};
                     d = cluster_draw(pw, lo, hi, u, tile_sum, sc, phase);
                 }
             } else {
-                const StagedP<TDT> pw{tb, lo, c, ps.t.m, inv_st};
+                const InFlight<StagedP<TDT>, 4> pw{{tb, lo, c, ps.t.m, inv_st}};
                 d = cluster_draw(pw, lo, hi, u, tile_sum, sc, phase);
             }
             if (d.failed || d.owner < 0) bad = true;

@@ -806,6 +806,13 @@ struct TilesInFlight<T, decltype((void)T::kTilesInFlight)> {
     static constexpr int value = T::kTilesInFlight;
 };
 
+// A weight functor with TB tiles in flight per warp, for kernels whose draw is bound by
+// latency rather than by the exp2 pipe (one CTA per SM).
+template <class WF, int TB>
+struct InFlight : WF {
+    static constexpr int kTilesInFlight = TB;
+};
+
 template <class WF>
 __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float* tile_sum, BlockScratch& sc,
                                    int& phase, int fail_in = 0) {

@@ -58,6 +58,19 @@ def test_mixed_batch_full_size():
     assert np.array_equal(g["tokens"][greedy], o["tokens"][greedy])  # greedy rows are exact
 
 
+@pytest.mark.parametrize("B,V", [(200, 40008), (160, 16392), (160, 152064)])
+def test_staged_walk_one_slot(B, V):
+    """Batches past one CTA per SM take the staged walk with a single slot (the next
+    position's chunk copied only once the current one is decided, warmed in L2 for
+    large chunks): ragged last CTAs, greedy and sampling rows, bf16 target and draft
+    logits."""
+    w = synth.mixed_batch(seed=B + V, B=B, K=4, V=V)
+    g, o = gpu_chain(w, seed=7, offset=2), oracle_chain(w, seed=7, offset=2)
+    assert compare(g, o) <= max(1, B // 200)
+    greedy = w["temperature"] <= 0
+    assert np.array_equal(g["tokens"][greedy], o["tokens"][greedy])
+
+
 @pytest.fixture(scope="module")
 def large_batch_sigma1():
     return synth.large_batch(seed=5, temperature=0.7, sigma=1.0)
