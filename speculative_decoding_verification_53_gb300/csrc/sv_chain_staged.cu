@@ -135,13 +135,6 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
         if (DK == DK_PROBS && !greedy && k < K && threadIdx.x == 0)
             qx_load = __ldg(reinterpret_cast<const float*>(dbase) + (size_t)k * V + x);
         const int fail = __syncthreads_or(!wait_slot(s));
-        // With a single slot the next position's copy can only start after this one is
-        // decided; for large chunks warm L2 with it now (speculative: wasted when x_k is
-        // rejected; measured a loss for chunks of 8 KB, a gain from 38 KB).
-        if (L.nslot == 1 && next_issue <= K && threadIdx.x == 0 && n * tsz >= 32 * 1024) {
-            prefetch_l2(tbase + ((size_t)next_issue * V + lo) * tsz, (uint32_t)n * tsz);
-            if (draft_rows && next_issue < K) prefetch_l2(dbase + ((size_t)next_issue * V + lo) * dsz, (uint32_t)n * dsz);
-        }
         if (DK == DK_PROBS && !greedy && k < K && threadIdx.x == 0) s_qx = qx_load;
         const unsigned char* tb = slots + (size_t)s * L.slot_bytes;
         const unsigned char* db = tb + L.t_bytes;
