@@ -100,13 +100,26 @@ def pinned(a):
 
 # ----------------------------------------------------------------- helpers
 
-def kernel_source_hash() -> str:
+# translation unit each profiled kernel is compiled from
+KERNEL_SOURCES = {"chain_spec_kernel": "sv_chain_spec.cu", "chain_staged_kernel": "sv_chain_staged.cu",
+                  "tree_staged_kernel": "sv_tree_staged.cu", "draft_sample_staged_kernel": "sv_sample.cu",
+                  "tree_mask_kernel": "sv_tree_kv.cu", "kv_compact_kernel": "sv_tree_kv.cu"}
+
+
+def kernel_source_hash(kernel: str = None) -> str:
+    """sha256 prefix of the device sources a kernel is compiled from: its translation
+    unit and the package's internal headers (.cuh, .h).  With no kernel (or one not
+    listed), every source file of the package and of include/."""
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "speculative_decoding_verification_53_gb300", "csrc")
-    for d in (pkg, os.path.join(ROOT, "include")):
-        for f in sorted(os.listdir(d)):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    if kernel in KERNEL_SOURCES:
+        files = [os.path.join(pkg, f) for f in sorted(os.listdir(pkg)) if f.endswith((".cuh", ".h"))]
+        files.append(os.path.join(pkg, KERNEL_SOURCES[kernel]))
+    else:
+        files = [os.path.join(d, f) for d in (pkg, os.path.join(ROOT, "include")) for f in sorted(os.listdir(d))]
+    for path in files:
+        with open(path, "rb") as fh:
+            h.update(os.path.basename(path).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -122,7 +135,7 @@ def measured_peak():
 
 def profile_traffic(workload: str, default_size: bool = True):
     """DRAM bytes per launch of the timed kernel from the committed ncu summary for this
-    workload (profiles/<kernel>_<workload>.md), if the kernel sources still hash to the
+    workload (profiles/<kernel>_<workload>.md), if that kernel's sources still hash to the
     value recorded there and the run uses the workload's default size and temperature
     (the summaries describe that configuration); else None.  Returns (bytes, summary
     path, kernel name)."""
@@ -133,7 +146,7 @@ def profile_traffic(workload: str, default_size: bool = True):
         hm = re.search(r"^kernel_source_sha:\s*([0-9a-f]+)", text, re.M)
         km = re.search(r"^kernel:\s*(\S+)", text, re.M)
         kernel = km.group(1) if km else None
-        if not m or not hm or hm.group(1) != kernel_source_hash() or not default_size:
+        if not m or not hm or hm.group(1) != kernel_source_hash(kernel) or not default_size:
             return None, os.path.relpath(path, ROOT), kernel
         return float(m.group(1)), os.path.relpath(path, ROOT), kernel
     return None, None, None

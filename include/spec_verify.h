@@ -73,7 +73,7 @@ typedef enum {
     SV_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles (size limits, device) */
     SV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
     SV_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up; the workspace must be re-zeroed */
-    SV_ERR_BAD_INPUT = 5    /* reserved for data errors reported through a status query */
+    SV_ERR_BAD_INPUT = 5    /* some batch rows held invalid data (see spec_verify_count_invalid) */
 } sv_status;
 
 typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -239,6 +239,22 @@ SV_API const char *spec_verify_status_string(sv_status status);
 /* Description of the CUDA error behind the most recent SV_ERR_CUDA returned on the
  * calling thread ("no CUDA error" if there was none).  Static storage; not freed. */
 SV_API const char *spec_verify_last_cuda_error(void);
+
+/*
+ * Data-error status of a finished verify call.  The verify entries report bad data
+ * per batch row, as out_count[b] = 0 (NaN or +inf in a row the rule read, a row with
+ * no finite logit, an out-of-range token, a malformed tree), and still process the
+ * other rows; they return SV_OK for such calls.  This counts those rows on the
+ * device, in stream order after the call: a non-zero count is the call's
+ * SV_ERR_BAD_INPUT, and the rows are the ones whose count is 0.
+ *   out_count    device int32 [B], as written by spec_verify_chain(_noalloc),
+ *                spec_greedy_accept, spec_verify_tree(_rule) or spec_sample_and_verify.
+ *   B            0 <= B <= 1<<24.
+ *   out_invalid  device int32, written once (no initialisation needed).
+ * One kernel on `stream`; nothing is allocated.  Errors: SV_ERR_INVALID_ARG (B out of
+ * range, out_invalid NULL, out_count NULL with B > 0), SV_ERR_CUDA (launch failure).
+ */
+SV_API sv_status spec_verify_count_invalid(const int32_t *out_count, int B, int32_t *out_invalid, void *stream);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,8 @@ SV_SIBLINGS_WITHOUT_REPLACEMENT, SV_SIBLINGS_IID = 0, 1
 
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_chain", "spec_greedy_accept", "spec_verify_tree",
            "spec_verify_status_string", "spec_verify_last_cuda_error", "spec_verify_chain_noalloc",
-           "spec_tree_mask", "spec_kv_compact", "spec_verify_tree_rule", "spec_sample_and_verify")
+           "spec_tree_mask", "spec_kv_compact", "spec_verify_tree_rule", "spec_sample_and_verify",
+           "spec_verify_count_invalid")
 
 _lib = None
 
@@ -73,6 +74,8 @@ def lib() -> ctypes.CDLL:
     L.spec_verify_status_string.restype = ctypes.c_char_p
     L.spec_verify_last_cuda_error.argtypes = []
     L.spec_verify_last_cuda_error.restype = ctypes.c_char_p
+    L.spec_verify_count_invalid.argtypes = [vp, ci, vp, vp]
+    L.spec_verify_count_invalid.restype = ci
     _lib = L
     return L
 
@@ -312,6 +315,27 @@ def spec_verify_tree(target_logits, draft, node_tokens, parent, temperature, max
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_tree")
     return out_tokens, out_count, out_path
+
+
+def spec_verify_count_invalid(out_count, *, out_invalid=None, stream=None):
+    """Number of invalid batch rows (out_count == 0) of a finished verify call, counted
+    on the device in stream order; returns an int32 device tensor of one element."""
+    torch = _torch()
+    _dev(out_count, "out_count", torch.int32)
+    if out_invalid is None:
+        out_invalid = torch.empty((1,), dtype=torch.int32, device=out_count.device)
+    st = lib().spec_verify_count_invalid(_ptr(out_count), out_count.numel(), _ptr(out_invalid), _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_count_invalid")
+    return out_invalid
+
+
+def rows_status(out_count, *, stream=None) -> int:
+    """SV_ERR_BAD_INPUT if any batch row of a finished verify call is invalid, else
+    SV_OK (reads one int32 back, so it waits for the stream)."""
+    n = spec_verify_count_invalid(out_count, stream=stream)
+    (_torch().cuda.current_stream() if stream is None else stream).synchronize()
+    return SV_ERR_BAD_INPUT if int(n.cpu().item()) > 0 else SV_OK
 
 
 def spec_tree_mask(parent, *, out_mask=None, out_depth=None, out_valid=None, stream=None):

@@ -79,6 +79,12 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert t(vp, 0, vp, 0, 1, vp, vp, vp, 1, 8, 100, 65, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
     assert t(vp, 0, vp, 0, 1, vp, vp, vp, 1, 1025, 100, 4, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
     assert t(vp, 0, vp, 0, 1, vp, None, vp, 1, 8, 100, 4, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    c = lib.spec_verify_count_invalid
+    # negative B, B over 2^24, no output, no counts with B > 0
+    assert c(vp, -1, vp, None) == sv.SV_ERR_INVALID_ARG
+    assert c(vp, (1 << 24) + 1, vp, None) == sv.SV_ERR_INVALID_ARG
+    assert c(vp, 4, None, None) == sv.SV_ERR_INVALID_ARG
+    assert c(None, 4, vp, None) == sv.SV_ERR_INVALID_ARG
 
 
 def test_binding_refuses_to_run_without_the_library(monkeypatch, tmp_path):

@@ -220,6 +220,28 @@ def test_masked_invalid_and_zero_q_rows():
     assert (g["count"] == 4).all()
 
 
+def test_count_invalid_rows_status():
+    """spec_verify_count_invalid counts the rows with count 0; rows_status turns a
+    non-zero count into SV_ERR_BAD_INPUT."""
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    w = synth.tiny_chain(seed=2, V=700, K=3, B=12)
+    t = w["target"].copy()
+    t[0, 0, 3] = np.nan
+    t[1, 0, :] = -np.inf
+    g = gpu_chain(dict(w, target=t))
+    cnt = torch.from_numpy(g["count"]).cuda()
+    assert int(sv.spec_verify_count_invalid(cnt).item()) == int((g["count"] == 0).sum()) == 2
+    assert sv.rows_status(cnt) == sv.SV_ERR_BAD_INPUT
+    assert sv.rows_status(torch.from_numpy(gpu_chain(w)["count"]).cuda()) == sv.SV_OK
+    rng = np.random.default_rng(4)
+    for B in (0, 1, 1023, 1024, 1025, 300001):
+        c = rng.integers(0, 3, B).astype(np.int32)
+        got = sv.spec_verify_count_invalid(torch.from_numpy(c).cuda()) if B else \
+            sv.spec_verify_count_invalid(torch.zeros(0, dtype=torch.int32, device="cuda"))
+        assert int(got.item()) == int((c == 0).sum())
+
+
 def _bad_after_first_rejection():
     """Rows whose first draft is surely rejected (p(x_0) = 0, or x_0 != argmax on greedy
     rows) carry invalid data only at later positions, which the rule never reads."""
