@@ -123,6 +123,23 @@ def kernel_source_hash(kernel: str = None) -> str:
     return h.hexdigest()[:16]
 
 
+def slowest_rank_ms(elapsed_ms: float, world: int, device) -> float:
+    """Length of the timed region on the slowest rank: the max over ranks (every rank
+    gets it).  `device` is where the collective's tensor lives (CUDA under NCCL, CPU
+    under gloo)."""
+    import torch
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Units all ranks processed (each its own, the same count per step) per second of
+    the slowest rank's timed region."""
+    return units_per_step * steps * world / (max_ms / 1e3)
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -358,13 +375,9 @@ def run_ours(args, rank, world, device):
     bytes_per_launch = float(np.mean(bytes_steps))
     mean_count = float(counts.mean())
 
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = slowest_rank_ms(elapsed_ms, world, device)
     ms_per_step = max_ms / args.steps
-    rows_total = per_step_rows * args.steps * world
-    value = rows_total / (max_ms / 1e3)
+    value = whole_job_rate(per_step_rows, args.steps, world, max_ms)
 
     # end to end: host buffers, copies inside the timed region, through the public API
     e2e = run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind)
@@ -666,12 +679,9 @@ def run_aux(args, rank, world, device):
             graphs[0][0].replay()
             torch.cuda.synchronize(device)
     clock = clocks.summary()
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = slowest_rank_ms(elapsed_ms, world, device)
     ms_per_step = max_ms / args.steps
-    value = a["per_step"] * args.steps * world / (max_ms / 1e3)
+    value = whole_job_rate(a["per_step"], args.steps, world, max_ms)
     bytes_per_launch = float(np.mean([bytes_of(i) for i in range(chunk)]))
     e2e = run_aux_e2e(args, a, device, stream)
     cpu = run_aux_cpu(args, a, budget_s=10.0) if (rank == 0 and not args.no_cpu_baseline) else None
