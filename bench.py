@@ -421,45 +421,75 @@ def run_ours(args, rank, world, device):
     return line
 
 
+def _packed(arrays, device):
+    """One pinned host buffer holding the arrays back to back (16-byte aligned offsets),
+    a device buffer of the same size, and device views of each array in it."""
+    import torch
+    parts, off = [], 0
+    for a in arrays:
+        a = np.ascontiguousarray(a)
+        parts.append((off, a))
+        off += (a.nbytes + 15) // 16 * 16
+    host = torch.zeros(off, dtype=torch.uint8).pin_memory()
+    hv = host.numpy()
+    dev = torch.empty(off, dtype=torch.uint8, device=device)
+    views = []
+    for o, a in parts:
+        hv[o:o + a.nbytes] = np.frombuffer(a.tobytes(), dtype=np.uint8)
+        dt = torch.bfloat16 if a.dtype == np.uint16 else getattr(torch, a.dtype.name)
+        views.append(dev[o:o + a.nbytes].view(dt).view(a.shape))
+    return host, dev, views
+
+
 def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
+    """Through the public API with host buffers, every step: the step's inputs copied from
+    pinned host memory (staged back to back, one copy), the verify call (outputs and
+    workspace preallocated, as a serving loop would), the tokens and counts copied back
+    to pinned host memory (one copy).  No synchronisation inside the loop."""
     import torch
     import speculative_decoding_verification_53_gb300 as sv
     n = min(args.e2e_steps, max(args.steps, 3))
     sl = slice(0, per_step_rows)
-    ht, hd = pinned(w["target"][sl]), pinned(w["draft"][sl])
-    htemp = pinned(w["temperature"][sl])
-    dt = torch.empty(ht.shape, dtype=ht.dtype, device=device)
-    dd = torch.empty(hd.shape, dtype=hd.dtype, device=device)
-    dtemp = torch.empty(htemp.shape, dtype=htemp.dtype, device=device)
     if tree:
-        htok, hpar = pinned(w["node_tokens"][sl]), pinned(w["parent"][sl])
-        dtok = torch.empty(htok.shape, dtype=torch.int32, device=device)
-        dpar = torch.empty(hpar.shape, dtype=torch.int32, device=device)
+        names = ["target", "draft", "node_tokens", "parent", "temperature"]
         D = w["max_depth"]
-        ho_t = torch.empty((per_step_rows, D + 1), dtype=torch.int32).pin_memory()
+        out_cols = D + 1
+    elif w.get("sample"):  # the drafted tokens are an output here
+        names = ["target", "draft", "temperature"]
+        out_cols = w["tokens"].shape[1] + 1
     else:
-        htok = pinned(w["tokens"][sl])
-        dtok = torch.empty(htok.shape, dtype=torch.int32, device=device)
-        ho_t = torch.empty((per_step_rows, htok.shape[1] + 1), dtype=torch.int32).pin_memory()
-    ho_c = torch.empty((per_step_rows,), dtype=torch.int32).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in ([ht, hd, htok, htemp] + ([hpar] if tree else [])))
-    d2h = ho_t.numel() * 4 + ho_c.numel() * 4
+        names = ["target", "draft", "tokens", "temperature"]
+        out_cols = w["tokens"].shape[1] + 1
+    hin, din, views = _packed([w[k][sl] for k in names], device)
+    # outputs back to back in one device buffer: tokens [B][cols], count [B] (and the
+    # tree's path, not read back)
+    dout = torch.empty(per_step_rows * (out_cols + 1), dtype=torch.int32, device=device)
+    ot = dout[:per_step_rows * out_cols].view(per_step_rows, out_cols)
+    oc = dout[per_step_rows * out_cols:]
+    hout = torch.empty_like(dout, device="cpu").pin_memory()
+    opath = torch.empty((per_step_rows, D), dtype=torch.int32, device=device) if tree else None
+    odraft = torch.empty((per_step_rows, w["tokens"].shape[1]), dtype=torch.int32, device=device) \
+        if w.get("sample") else None
+    K = w["tokens"].shape[1] if not tree else 0
+    ws_bytes = sv.spec_verify_workspace_size(per_step_rows, K, w["target"].shape[2]) if not tree else 0
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=device) if not tree else None
 
     def one(i):
-        dt.copy_(ht, non_blocking=True)
-        dd.copy_(hd, non_blocking=True)
-        dtok.copy_(htok, non_blocking=True)
-        dtemp.copy_(htemp, non_blocking=True)
+        din.copy_(hin, non_blocking=True)
         if tree:
-            dpar.copy_(hpar, non_blocking=True)
-            ot, oc, _ = sv.spec_verify_tree(dt, dd, dtok, dpar, dtemp, D, 23, i, draft_kind=kind,
-                                            sibling_rule=w.get("sibling_rule", "without_replacement"))
+            dt, dd, dtok, dpar, dtemp = views
+            sv.spec_verify_tree(dt, dd, dtok, dpar, dtemp, D, 23, i, draft_kind=kind,
+                                sibling_rule=w.get("sibling_rule", "without_replacement"),
+                                out_tokens=ot, out_count=oc, out_path=opath)
         elif w.get("sample"):
-            _, ot, oc, _ = sv.spec_sample_and_verify(dt, dd, dtemp, 23, i)
+            dt, dd, dtemp = views
+            sv.spec_sample_and_verify(dt, dd, dtemp, 23, i, out_draft_tokens=odraft, out_tokens=ot, out_count=oc,
+                                      workspace=ws)
         else:
-            ot, oc, _ = sv.spec_verify_chain(dt, dd, dtok, dtemp, 23, i, draft_kind=kind)
-        ho_t.copy_(ot, non_blocking=True)
-        ho_c.copy_(oc, non_blocking=True)
+            dt, dd, dtok, dtemp = views
+            sv.spec_verify_chain(dt, dd, dtok, dtemp, 23, i, draft_kind=kind, out_tokens=ot, out_count=oc,
+                                 workspace=ws)
+        hout.copy_(dout, non_blocking=True)
 
     for i in range(3):
         one(i)
@@ -471,8 +501,14 @@ def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
     end.record(stream)
     torch.cuda.synchronize(device)
     ms = start.elapsed_time(end)
-    return {"value": per_step_rows * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": ms / n}
+    for k, v in zip(names, views):  # the staged views hold exactly the step's inputs
+        a = np.ascontiguousarray(w[k][sl])
+        got = v.cpu().view(torch.int16).numpy().view(np.uint16) if a.dtype == np.uint16 else v.cpu().numpy()
+        if not np.array_equal(got.view(np.uint8), a.view(np.uint8)):
+            raise RuntimeError(f"end-to-end staging of {k} is wrong")
+    return {"value": per_step_rows * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(hin.numel()),
+            "d2h_bytes_per_step": int(hout.numel() * 4), "steps": n, "ms_per_step": ms / n,
+            "staging": "inputs packed in one pinned buffer (one copy in), tokens and counts in one (one copy out)"}
 
 
 def run_cpu_baseline(w, per_step_rows, n_inputs, tree, budget_s=10.0):
