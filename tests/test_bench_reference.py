@@ -1,0 +1,31 @@
+"""bench.py's reference arm (the oracle timed on the host cores) prints the contract's
+JSON line; it needs no GPU, so it runs here on small samples of two workloads."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+REQUIRED = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+            "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"}
+
+
+@pytest.mark.parametrize("extra,unit", [(["--workload", "single_stream", "--rounds", "2"], "verify rows/s"),
+                                        (["--workload", "tree_mask", "--batch", "8", "--nodes", "60"], "trees/s")])
+def test_reference_arm_prints_the_contract_line(extra, unit):
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3", *extra],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert REQUIRED <= set(line)
+    assert line["impl"] == "reference" and line["unit"] == unit and line["value"] > 0
+    assert line["higher_is_better"] is True and line["data"] == "synthetic"
+    assert line["steps"] == 2 and line["warmup"] >= 3
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == unit
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    assert "workload" in line["config"]
