@@ -115,12 +115,31 @@ sv::StageLayout chain_stage_layout(const void* target, int tdt, const void* draf
     return L;
 }
 
-// Cluster size of the position-parallel kernel: the largest power of two (at most 16)
-// that keeps B * (K + 1) clusters within one CTA per SM.
-int spec_cluster(int B, int K, int num_sms) {
+// Cluster size of the position-parallel kernel, or 0 where the walking kernels are
+// faster:
+//  - one CTA per SM when the batch allows a cluster of at least 4: the largest power of
+//    two (at most 16) with B (K + 1) G <= SMs;
+//  - else a cluster that leaves each CTA 12 K to 24 K elements (G >= 2), when the
+//    launch fits in two waves of CTAs (how many fit on an SM set by the kernel's shared
+//    memory, at most four).  Measured against the staged walk, K = 5: V = 32000 at G = 2,
+//    B = 16 / 32 / 64: 10.5 / 11.4 / 17.4 us against 16.5 / 18.3 / 20.1; V = 128256 at
+//    G = 8, B = 8 / 16: 11.5 / 17.6 against 16.7 / 21.2; at B = 128 (3.4 waves) 29.7
+//    against 28.2.  Where it runs, every position is read, the rejected ones included.
+//  forced: the kernel was requested (SPEC_VERIFY_PATH=spec, the allocation-free entry);
+//  the one-CTA-per-SM size is used when the rules above give none.
+int spec_cluster(int B, int K, int V, int tsz, int dsz, int num_sms, bool forced) {
     int G = 16;
     while (G > 1 && (long long)B * (K + 1) * G > num_sms) G >>= 1;
-    return G;
+    if (G >= 4) return G;
+    int Gc = 1;
+    while (Gc < 16 && (long long)V >= 2LL * Gc * 12288) Gc *= 2;
+    if (Gc >= 2) {
+        const size_t smem = sv::spec_smem_bytes(V, Gc, tsz, dsz, nullptr, nullptr) + 8192;  // + static, reserved
+        long long fit = (long long)(232448 / smem);
+        if (fit > 4) fit = 4;
+        if (fit >= 1 && (long long)B * (K + 1) * Gc <= 2LL * fit * num_sms) return Gc;
+    }
+    return forced ? G : 0;
 }
 
 // Kernel choice for a chain launch:
@@ -148,8 +167,8 @@ sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_
     }
     if ((path == PATH_AUTO || path == PATH_SPEC) && aligned && ws && ((uintptr_t)ws & 255u) == 0 &&
         a.K + 1 <= sv::SPEC_MAX_POS) {
-        const int Gs = spec_cluster(a.B, a.K, num_sms);
-        if ((path == PATH_SPEC || Gs >= 4) && ws_bytes >= sv::spec_workspace_bytes(a.B, a.K, a.V, Gs)) {
+        const int Gs = spec_cluster(a.B, a.K, a.V, (int)tsz, (int)dsz, num_sms, path == PATH_SPEC);
+        if (Gs > 0 && ws_bytes >= sv::spec_workspace_bytes(a.B, a.K, a.V, Gs)) {
             const cudaError_t e = sv::launch_chain_spec(a, ws, tdt, ddt, dk, Gs, stream);
             if (e == cudaSuccess) return SV_OK;
             if (e != cudaErrorInvalidClusterSize) return launch_status(e);
