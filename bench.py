@@ -415,7 +415,7 @@ def run_ours(args, rank, world, device):
                      "traffic_source": prof},
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if w.get("sample") else 1),  # sampling + verify kernels per step
         "clocks": clock,
     }
     return line
