@@ -71,6 +71,26 @@ def test_staged_walk_one_slot(B, V):
     assert np.array_equal(g["tokens"][greedy], o["tokens"][greedy])
 
 
+def test_moderate_batch_position_parallel_with_bad_rows():
+    """B = 32, V = 32000: the automatic path runs the position-parallel kernel in
+    clusters of 2 over two waves.  Rows carry NaN, +inf, all -inf or an out-of-range
+    token at various positions; only data the rule reads may invalidate a row."""
+    w = synth.mixed_batch(seed=77, B=32, K=5, V=32000)
+    t, d, toks = w["target"].copy(), w["draft"].copy(), w["tokens"].copy()
+    nan, inf, ninf = np.uint16(0x7FC0), np.uint16(0x7F80), np.uint16(0xFF80)  # bf16 bit patterns
+    t[0, 0, 11] = nan
+    t[1, 3, 5] = inf
+    t[2, 5, :] = ninf
+    d[3, 1, 7] = nan
+    toks[4, 2] = 32000
+    toks[5, 0] = -3
+    t[6, 2, :16000] = ninf  # half masked: still valid
+    w2 = dict(w, target=t, draft=d, tokens=toks)
+    g, o = gpu_chain(w2, seed=5, offset=1), oracle_chain(w2, seed=5, offset=1)
+    assert compare(g, o) <= 1
+    assert g["count"][4] == 0 and g["count"][5] == 0 and g["count"][0] == 0
+
+
 @pytest.fixture(scope="module")
 def large_batch_sigma1():
     return synth.large_batch(seed=5, temperature=0.7, sigma=1.0)
