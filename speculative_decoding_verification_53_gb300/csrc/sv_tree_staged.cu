@@ -86,7 +86,7 @@ struct StagedNodeP {
 constexpr int TREE_GATHER = 64;  // children whose raw values are prefetched at node entry
 
 template <int TDT, int DDT, int DK>
-__global__ void __launch_bounds__(NT) tree_staged_kernel(const TreeArgs a, const StageLayout L) {
+__global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, const StageLayout L) {
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ BlockScratch sc;
     __shared__ float s_rt[TREE_GATHER], s_rd[TREE_GATHER];
