@@ -143,8 +143,10 @@ int spec_cluster(int B, int K, int V, int tsz, int dsz, int num_sms, bool forced
 }
 
 // Kernel choice for a chain launch:
-//  - position-parallel (sv_chain_spec.cu) for small batches when a workspace is given:
-//    every position of every row at once, the latency of one position instead of K+1;
+//  - position-parallel (sv_chain_spec.cu) for small and moderate batches when a workspace
+//    is given (spec_cluster): every position of every row at once, the latency of one
+//    position instead of K+1, at the price of reading the positions after the first
+//    rejection;
 //  - shared-memory staged walk (sv_chain_staged.cu) when rows are 16-byte aligned;
 //  - register-streaming walk (sv_chain.cu) otherwise.
 sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_draft, int num_sms, void* ws,
