@@ -193,6 +193,24 @@ def test_draft_length_extremes(K):
     assert compare(gpu_chain(w), oracle_chain(w)) <= 1
 
 
+def test_position_parallel_at_its_26_position_limit():
+    """K = 25 puts 26 positions into the position-parallel kernel's packed arrival word
+    (reject bits 11..36, invalid bits 37..62; B = 1 with aligned rows takes that kernel).
+    Near-certain acceptance reaches the last positions; a NaN in the bonus row makes
+    exactly the rounds that reach it invalid.  K = 26 is past the limit and walks."""
+    for K in (25, 26):
+        excused = 0
+        for s in range(8):
+            w = synth.tiny_chain(seed=100 + s, V=1024, K=K, B=1, temperature=1.0, sigma=0.05)
+            if s >= 4:
+                t = w["target"].copy()
+                t[0, K, 7] = np.nan
+                w = dict(w, target=t)
+            g, o = gpu_chain(w, seed=s, offset=s), oracle_chain(w, seed=s, offset=s)
+            excused += compare(g, o)
+        assert excused <= 1
+
+
 def test_greedy_ties_and_entry_point():
     import speculative_decoding_verification_53_gb300 as sv
     rng = np.random.default_rng(8)
