@@ -108,7 +108,10 @@ SV_API size_t spec_verify_workspace_size(int B, int K, int V);
  *                  1 for a match, 0 for the mismatch); -1 for positions never
  *                  evaluated.
  *   workspace, ws_bytes  optional scratch (see spec_verify_workspace_size).
- * Rows after the first rejection are never read.
+ * Rows after the first rejection never affect the result and are not validated
+ * (invalid data there leaves the row valid).  With a workspace, small and moderate
+ * batches run a kernel that reads every position at once to shorten the critical
+ * path; the other kernels stop reading at the first rejection.
  */
 SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt,
                             const void *draft, sv_dtype ddt, sv_draft_kind dk,
