@@ -13,6 +13,15 @@ residual, the greedy case); "Progressive Tree Drafting", section "검증"
 
 Array conventions: logits are numpy ``float32`` (fp32) or ``uint16`` holding
 bfloat16 bit patterns; draft probabilities are ``float32``.
+
+Pins (tests/test_oracle_pins.py, test_oracle_mask_kv.py, test_oracle_sample.py):
+every function is checked against something other than itself -- numpy's Philox,
+closed forms, numpy argmax / searchsorted, exact law enumeration, the printed
+expected-token value, brute-force tree paths, networkx ancestor sets, a gather
+from the unmodified cache.  Parity unpinned: tree sampling on trees whose children
+are a parent's top draft tokens (a deterministic choice, not a draw from q) has no
+law to compare with; there ``verify_tree`` is checked only through the cases above
+(trees drawn without replacement or i.i.d., chains as trees, greedy trees).
 """
 from __future__ import annotations
 
