@@ -8,7 +8,9 @@ its own arithmetic:
   the slot layout making the two walks consume the same uniforms;
 - identical draft and target distributions accept every draft (ratio 1 > r);
 - drafts outside the target's support are rejected at once, and the replacement lies
-  in the support.
+  in the support;
+- the tree mask of any valid parent array is each node's ancestor-or-self set;
+- the compaction of any root-to-node path is a gather from the unmodified cache.
 """
 import numpy as np
 import pytest
@@ -96,3 +98,48 @@ def test_drafts_outside_the_target_support_are_rejected_at_once(c):
     o = oracle.verify_chain(t, d, toks, temps, seed, 2)
     assert (o["count"] == 1).all()
     assert (o["tokens"][:, 0] < half).all()
+
+
+@settings(max_examples=120, deadline=None)
+@given(st.integers(0, 10_000), st.integers(1, 70))
+def test_mask_is_the_ancestor_or_self_set(seed, N):
+    """Any valid parent array (parent[i] in {-1} u [0, i)): bit j of row i is set iff j
+    is i or an ancestor of i; depth is the number of nodes from the root's child down."""
+    rng = np.random.default_rng(seed)
+    par = np.array([[rng.integers(-1, i) if i else -1 for i in range(N)]], np.int32)
+    o = oracle.tree_mask(par)
+    assert o["valid"][0] == 1
+    for i in range(N):
+        anc, a = {i}, par[0, i]
+        while a >= 0:
+            anc.add(int(a))
+            a = par[0, a]
+        bits = {j for j in range(N) if (int(o["mask"][0, i, j // 32]) >> (j % 32)) & 1}
+        assert bits == anc
+        assert o["depth"][0, i] == len(anc)
+
+
+@settings(max_examples=120, deadline=None)
+@given(st.integers(0, 10_000), st.integers(2, 40), st.integers(1, 6))
+def test_compaction_is_a_gather_from_the_original_cache(seed, N, D):
+    """A root-to-node path (increasing node indices): rows base+d take the original rows
+    base+path[d] for d < count-1; every other row is untouched."""
+    rng = np.random.default_rng(seed)
+    par = np.array([[rng.integers(-1, i) if i else -1 for i in range(N)]], np.int32)
+    node = int(rng.integers(0, N))
+    chain = []
+    while node >= 0:
+        chain.append(node)
+        node = par[0, node]
+    chain = chain[::-1][:D]
+    path = np.full((1, D), -1, np.int32)
+    path[0, :len(chain)] = chain
+    count = np.array([len(chain) + 1], np.int32)
+    R, rb = N + 8, 12
+    base = np.array([int(rng.integers(0, R - N + 1))], np.int32)
+    kv = rng.integers(0, 256, (1, R, rb), dtype=np.uint8)
+    out = oracle.kv_compact(kv, path, count, base)
+    want = kv.copy()
+    for d, v in enumerate(chain):
+        want[0, base[0] + d] = kv[0, base[0] + v]
+    assert (out == want).all()
