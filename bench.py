@@ -16,12 +16,16 @@ tree_mask and kv_compact time the steps on either side of a tree verify (the
 ancestor attention mask of each draft tree; moving the accepted branch's KV-cache
 rows to the front) with their own metric and unit.
 
-Prints one JSON line (rank 0).  `value` is verify rows/s over all ranks;
-`roofline` relates the kernel's algorithmic bytes per launch (the rows the rule
-needs: target rows up to the first rejection, gathered draft entries, the draft
-row of the rejected position) to its event-timed duration; `e2e` is the same
-metric through the public API with host buffers (copies inside the timed
-region); `cpu_baseline` is the fp64 oracle on a bounded sample, single thread.
+Prints one JSON line (rank 0).  `value` is verify rows/s over all ranks (under
+torchrun every rank is an independent replica on its own rows; the time is the
+slowest rank's); `roofline` relates the kernel's algorithmic bytes per launch
+(the rows the rule needs: target rows up to the first rejection, gathered draft
+entries, the draft row of the rejected position) to its event-timed duration,
+and `roofline.traffic` is the DRAM bytes per launch from the committed ncu
+summary of that kernel (null once the kernel's sources have changed); `e2e` is
+the same metric through the public API with host buffers (copies inside the
+timed region); `cpu_baseline` is the fp64 oracle on a bounded sample, single
+thread.
 """
 from __future__ import annotations
 
