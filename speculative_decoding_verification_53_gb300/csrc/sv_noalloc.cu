@@ -52,9 +52,16 @@ sv_status spec_verify_chain_noalloc(const void* target_logits, sv_dtype tdt, con
                                     sv_draft_kind dk, const int32_t* draft_tokens, const float* temperature, int B,
                                     int K, int V, uint64_t seed, uint64_t offset, int32_t* out_tokens,
                                     int32_t* out_count, float* out_accept_prob, void* stream) {
+    // the argument checks of spec_verify_chain, before anything touches the device
     if (B < 0 || K < 0 || V < 1) return SV_ERR_INVALID_ARG;
-    if (spec_verify_workspace_size(B, K, V) > NOALLOC_SCRATCH_BYTES) return SV_ERR_UNSUPPORTED;
+    const size_t need = spec_verify_workspace_size(B, K, V);
+    if (B > 0 && need == 0) return SV_ERR_INVALID_ARG;  // K or V beyond the library's limits
+    if ((unsigned)tdt > 1u || (unsigned)ddt > 1u || (unsigned)dk > 1u) return SV_ERR_INVALID_ARG;
+    if (dk == SV_DRAFT_PROBS && ddt != SV_F32) return SV_ERR_INVALID_ARG;
+    if (need > NOALLOC_SCRATCH_BYTES) return SV_ERR_UNSUPPORTED;
     if (B == 0) return SV_OK;
+    if (!target_logits || !temperature || !out_tokens || !out_count || (K > 0 && (!draft_tokens || !draft)))
+        return SV_ERR_INVALID_ARG;
     void* scratch = nullptr;
     const sv_status st = scratch_for_current_device(&scratch);
     if (st != SV_OK) return st;

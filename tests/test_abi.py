@@ -79,6 +79,29 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert t(vp, 0, vp, 0, 1, vp, vp, vp, 1, 8, 100, 65, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
     assert t(vp, 0, vp, 0, 1, vp, vp, vp, 1, 1025, 100, 4, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
     assert t(vp, 0, vp, 0, 1, vp, None, vp, 1, 8, 100, 4, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    tr = lib.spec_verify_tree_rule
+    # an unknown sibling rule; draft probabilities with a bf16 draft dtype; an empty batch
+    assert tr(vp, 0, vp, 0, 1, vp, vp, vp, 1, 8, 100, 4, 2, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    assert tr(vp, 0, vp, 1, 0, vp, vp, vp, 1, 8, 100, 4, 0, 0, 0, vp, vp, vp, None) == sv.SV_ERR_INVALID_ARG
+    assert tr(None, 0, None, 0, 1, None, None, None, 0, 8, 100, 4, 1, 0, 0, None, None, None, None) == sv.SV_OK
+    sa = lib.spec_sample_and_verify
+    # negative B, a bad dtype, no draft logits or drafted-token output with K > 0, an empty batch
+    assert sa(vp, 0, vp, 0, vp, -1, 4, 100, 0, 0, vp, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert sa(vp, 0, vp, 5, vp, 1, 4, 100, 0, 0, vp, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert sa(vp, 0, None, 0, vp, 1, 4, 100, 0, 0, vp, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert sa(vp, 0, vp, 0, vp, 1, 4, 100, 0, 0, None, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert sa(None, 0, None, 0, None, 0, 4, 100, 0, 0, None, None, None, None, None, 0, None) == sv.SV_OK
+    na = lib.spec_verify_chain_noalloc
+    # checked like spec_verify_chain before the device is touched; scratch over 256 KiB is refused
+    assert na(vp, 0, vp, 0, 0, vp, vp, 1, 65, 100, 0, 0, vp, vp, None, None) == sv.SV_ERR_INVALID_ARG
+    assert na(vp, 7, vp, 0, 0, vp, vp, 1, 4, 100, 0, 0, vp, vp, None, None) == sv.SV_ERR_INVALID_ARG
+    assert na(vp, 0, vp, 1, 0, vp, vp, 1, 4, 100, 0, 0, vp, vp, None, None) == sv.SV_ERR_INVALID_ARG
+    assert na(None, 0, vp, 0, 0, vp, vp, 1, 4, 100, 0, 0, vp, vp, None, None) == sv.SV_ERR_INVALID_ARG
+    assert na(vp, 0, vp, 0, 0, vp, vp, 40000, 4, 100, 0, 0, vp, vp, None, None) == sv.SV_ERR_UNSUPPORTED
+    assert na(None, 0, None, 0, 0, None, None, 0, 4, 100, 0, 0, None, None, None, None) == sv.SV_OK
+    ws = lib.spec_verify_workspace_size
+    assert ws(-1, 4, 100) == 0 and ws(1, 65, 100) == 0 and ws(1, 4, 0) == 0
+    assert ws(1, 5, 128256) == 256 and ws(1000, 5, 128256) == 8192  # one 8-byte word per row, 256-byte rounded
     c = lib.spec_verify_count_invalid
     # negative B, B over 2^24, no output, no counts with B > 0
     assert c(vp, -1, vp, None) == sv.SV_ERR_INVALID_ARG
