@@ -609,3 +609,19 @@ def test_margin_reports_distance_to_decision():
     # ratio 0.5 accepted with margin 0.125; bonus draw from (1/2, 1/2) at t = 0.25 -> margin 0.25
     assert out["count"][0] == 2
     assert out["margin"][0] == pytest.approx(0.125, abs=1e-15)
+
+
+def test_draw_margin_is_the_distance_to_the_nearest_cdf_boundary_in_mass():
+    """Where the draw decides the margin: a bonus draw from p = (1/4)x4 at u = 0.26 lands
+    0.01 past the boundary 0.25; a residual draw from (p - q)+ = (0, 1/2) at u = 0.9
+    lands at t = u Z = 0.45, 0.05 (in mass, not divided by Z) below the boundary 0.5."""
+    out = oracle.verify_chain(np.zeros((1, 1, 4), np.float32), np.zeros((1, 0, 4), np.float32),
+                              np.zeros((1, 0), np.int32), np.ones(1, np.float32), 0, 0,
+                              draft_kind=oracle.DRAFT_PROBS, uniforms=(np.zeros((1, 0)), np.array([[0.26]])))
+    assert out["count"][0] == 1 and out["tokens"][0, 0] == 1
+    assert out["margin"][0] == pytest.approx(0.01, abs=1e-12)
+    out = oracle.verify_chain(np.zeros((1, 2, 2), np.float32), np.array([[[1.0, 0.0]]], np.float32),
+                              np.zeros((1, 1), np.int32), np.ones(1, np.float32), 0, 0,
+                              draft_kind=oracle.DRAFT_PROBS, uniforms=(np.array([[0.75]]), np.array([[0.9, 0.0]])))
+    assert out["count"][0] == 1 and out["tokens"][0, 0] == 1  # x = 0 rejected (ratio 1/2), residual draws 1
+    assert out["margin"][0] == pytest.approx(0.05, abs=1e-12)  # min(|0.75 - 0.5|, 0.05)
