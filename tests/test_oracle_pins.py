@@ -625,3 +625,30 @@ def test_draw_margin_is_the_distance_to_the_nearest_cdf_boundary_in_mass():
                               draft_kind=oracle.DRAFT_PROBS, uniforms=(np.array([[0.75]]), np.array([[0.9, 0.0]])))
     assert out["count"][0] == 1 and out["tokens"][0, 0] == 1  # x = 0 rejected (ratio 1/2), residual draws 1
     assert out["margin"][0] == pytest.approx(0.05, abs=1e-12)  # min(|0.75 - 0.5|, 0.05)
+
+
+def test_accept_prob_layout_after_the_first_rejection_and_on_greedy_rows():
+    """Sampling rows: min(1, p/q) up to and including the first rejection, -1 after it.
+    Greedy rows: 1 for each match, 0 for the mismatch, -1 after it."""
+    V, K = 3, 3
+    target = np.zeros((2, K + 1, V), np.float32)
+    target[1, :, 2] = 5.0  # greedy row: argmax 2 at every position
+    draft = np.full((2, K, V), 1.0 / 3, np.float32)
+    toks = np.array([[0, 1, 2], [2, 0, 2]], np.int32)
+    r = np.array([[0.5, 0.9999, 0.0], [0.0, 0.0, 0.0]])  # row 0: ratio 1 at every position
+    u = np.zeros((2, K + 1))
+    out = oracle.verify_chain(target, draft, toks, np.array([1.0, 0.0], np.float32), 0, 0,
+                              draft_kind=oracle.DRAFT_PROBS, uniforms=(r, u))
+    # row 0: p = q = 1/3, ratio 1 > r: all accepted, then the bonus token
+    assert out["count"][0] == K + 1
+    np.testing.assert_array_equal(out["accept_prob"][0], [1.0, 1.0, 1.0])
+    # row 1 (greedy): x_0 = 2 matches, x_1 = 0 does not -> emits 2; position 2 never evaluated
+    assert out["count"][1] == 2 and list(out["tokens"][1, :2]) == [2, 2]
+    np.testing.assert_array_equal(out["accept_prob"][1], [1.0, 0.0, -1.0])
+    # a sampling row rejected at position 1 reports min(1, p/q) there and -1 after it
+    target2 = np.zeros((1, K + 1, V), np.float32)
+    target2[0, 1, 0] = -np.inf  # p_1(0) = 0, so x_1 = 0 is rejected (ratio 0)
+    out = oracle.verify_chain(target2, draft[:1], np.array([[1, 0, 1]], np.int32), np.ones(1, np.float32), 0, 0,
+                              draft_kind=oracle.DRAFT_PROBS, uniforms=(np.array([[0.3, 0.3, 0.3]]), np.zeros((1, K + 1))))
+    assert out["count"][0] == 2
+    np.testing.assert_array_equal(out["accept_prob"][0], [1.0, 0.0, -1.0])
