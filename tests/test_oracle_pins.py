@@ -652,3 +652,19 @@ def test_accept_prob_layout_after_the_first_rejection_and_on_greedy_rows():
                               draft_kind=oracle.DRAFT_PROBS, uniforms=(np.array([[0.3, 0.3, 0.3]]), np.zeros((1, K + 1))))
     assert out["count"][0] == 2
     np.testing.assert_array_equal(out["accept_prob"][0], [1.0, 0.0, -1.0])
+
+
+def test_tree_margin_and_sibling_update_worked_example():
+    """Root p = (1/2, 1/2), q = (3/4, 1/4); children x = 0 then x = 1.  Child 0: ratio 2/3,
+    r = 0.9 rejects (margin 0.2333).  Then p <- (p - q)+ / Z = (0, 1), q(0) <- 0 and
+    q <- q / sum q = (0, 1), so child 1 has ratio 1 and r = 0.4 accepts (margin 0.6).  Child
+    1 is a leaf: the last token is drawn from its row p = (1/2, 1/2) at u = 0.7 -> token 1,
+    margin 0.2.  The row's margin is the smallest, 0.2."""
+    target = np.zeros((1, 3, 2), np.float32)
+    draft = np.array([[[0.75, 0.25], [0.5, 0.5], [0.5, 0.5]]], np.float32)
+    out = oracle.verify_tree(target, draft, np.array([[0, 1]], np.int32), np.array([[-1, -1]], np.int32),
+                             np.ones(1, np.float32), 1, 0, 0, draft_kind=oracle.DRAFT_PROBS,
+                             uniforms=(np.array([[0.9, 0.4]]), np.array([[0.0, 0.0, 0.7]])))
+    assert out["count"][0] == 2
+    assert list(out["tokens"][0]) == [1, 1] and list(out["path"][0]) == [1]
+    assert out["margin"][0] == pytest.approx(0.2, abs=1e-12)
