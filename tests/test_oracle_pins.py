@@ -162,11 +162,15 @@ def test_bonus_draw_matches_searchsorted():
 
 
 def test_disjoint_supports_give_one_token_from_p():
-    """q and p on disjoint supports: every draft is rejected and the replacement (the residual
-    is p itself) always lies in p's support."""
+    """q and p on disjoint supports: every draft is rejected, the replacement (the residual
+    is p itself) always lies in p's support, and it is distributed as p_0.  Every row
+    shares one target row 0, so the B replacements are B draws from one law, checked by a
+    chi-square test over the half support (7 degrees of freedom; 24.32 is the 0.999
+    quantile of that law)."""
     rng = np.random.default_rng(13)
-    B, K, V = 500, 4, 16
+    B, K, V = 4000, 4, 16
     target = rng.normal(0, 1, (B, K + 1, V)).astype(np.float32)
+    target[:, 0] = rng.normal(0, 1, V).astype(np.float32)  # one row 0 for every batch row
     draft = rng.normal(0, 1, (B, K, V)).astype(np.float32)
     target[:, :, V // 2:] = -np.inf
     draft[:, :, : V // 2] = -np.inf
@@ -176,7 +180,13 @@ def test_disjoint_supports_give_one_token_from_p():
     assert (out["tokens"][:, 0] < V // 2).all() and (out["tokens"][:, 0] >= 0).all()
     # law of the replacement is p_0: chi-square over the half support
     counts = np.bincount(out["tokens"][:, 0], minlength=V)[: V // 2]
-    assert counts.sum() == B
+    p0 = softmax64(target[0, 0, : V // 2].astype(np.float64))
+    expected = B * p0
+    chi2 = float(((counts - expected) ** 2 / expected).sum())
+    assert chi2 < 24.32, (chi2, counts.tolist(), expected.round(1).tolist())
+    # the same statistic rejects a plausible slip: a replacement drawn uniformly over the support
+    uniform = np.full(V // 2, B / (V // 2))
+    assert float(((counts - uniform) ** 2 / uniform).sum()) > 24.32
 
 
 # ------------------------------------------- exact law on the uniform grid
