@@ -267,6 +267,230 @@ def algorithmic_bytes_tree(w, counts, paths):
 
 # ---------------------------------------------------------------- our arm
 
+L2_FLUSH_BYTES = 512 << 20  # written right before every timed region (the L2 holds 129 MB)
+
+
+def dense_bytes_chain(w, rows):
+    """Bytes of every row the verify could read, whatever the decisions: all K+1 target
+    rows, plus the K draft rows of sampling rows (logits), or the K gathered draft
+    probabilities and one draft row (probabilities)."""
+    target, draft = w["target"], w["draft"]
+    _, K1, V = target.shape
+    K = K1 - 1
+    tb, db = V * target.dtype.itemsize, V * draft.dtype.itemsize
+    total = 0
+    for b in rows:
+        total += K1 * tb
+        if w["temperature"][b] > 0 and K > 0:
+            total += K * db if w["draft_kind"] == 1 else K * 4 + db
+    return total
+
+
+def dense_bytes_tree(w):
+    """Every target row of every tree (the rows a level-by-level evaluation would read)."""
+    t = w["target"]
+    return t.shape[0] * t.shape[1] * t.shape[2] * t.dtype.itemsize
+
+
+class Timed:
+    """One workload resident on the device, its steps captured in CUDA graphs."""
+
+    def __init__(self, w, device, stream, steps, warmup, seed=17, dev_inputs=None):
+        import torch
+        import speculative_decoding_verification_53_gb300 as sv
+        self.w, self.device, self.stream, self.steps = w, device, stream, steps
+        self.tree = w["kind"] == "tree"
+        self.sample = bool(w.get("sample"))
+        rule = w.get("sibling_rule", "without_replacement")
+        rows = w["per_step_rows"]
+        if dev_inputs is None:
+            dev_inputs = {k: to_dev(w[k], device) for k in ("target", "draft")}
+        dt, dd = dev_inputs["target"], dev_inputs["draft"]
+        if self.tree:
+            dtok, dpar = to_dev(w["node_tokens"], device), to_dev(w["parent"], device)
+        else:
+            dtok = to_dev(w["tokens"], device)
+        dtemp = to_dev(w["temperature"], device)
+        kind = "probs" if w["draft_kind"] == 0 else "logits"
+        self.n_inputs = dt.shape[0] // rows
+        self.resident_bytes = int(dt.numel() * dt.element_size() + dd.numel() * dd.element_size())
+        chunk = min(steps, 1000)
+        self.chunk = chunk
+        if self.tree:
+            D = w["max_depth"]
+            out_t = torch.empty((chunk, rows, D + 1), dtype=torch.int32, device=device)
+            self.out_c = torch.empty((chunk, rows), dtype=torch.int32, device=device)
+            self.out_p = torch.empty((chunk, rows, D), dtype=torch.int32, device=device)
+        else:
+            K_ = w["tokens"].shape[1]
+            out_t = torch.empty((chunk, rows, K_ + 1), dtype=torch.int32, device=device)
+            self.out_c = torch.empty((chunk, rows), dtype=torch.int32, device=device)
+            out_x = torch.empty((chunk, rows, K_), dtype=torch.int32, device=device)
+            ws_bytes = sv.spec_verify_workspace_size(rows, K_, w["target"].shape[2])
+            ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+        n_inputs = self.n_inputs
+
+        def step(i, slot):
+            r = (i % n_inputs) * rows
+            sl = slice(r, r + rows)
+            if self.tree:
+                sv.spec_verify_tree(dt[sl], dd[sl], dtok[sl], dpar[sl], dtemp[sl], D, seed, i, draft_kind=kind,
+                                    out_tokens=out_t[slot], out_count=self.out_c[slot], out_path=self.out_p[slot],
+                                    sibling_rule=rule)
+            elif self.sample:
+                sv.spec_sample_and_verify(dt[sl], dd[sl], dtemp[sl], seed, i, out_draft_tokens=out_x[slot],
+                                          out_tokens=out_t[slot], out_count=self.out_c[slot], workspace=ws)
+            else:
+                sv.spec_verify_chain(dt[sl], dd[sl], dtok[sl], dtemp[sl], seed, i, draft_kind=kind,
+                                     out_tokens=out_t[slot], out_count=self.out_c[slot], workspace=ws)
+
+        with torch.cuda.stream(stream):
+            for i in range(max(warmup, 3)):
+                step(i, i % chunk)
+        torch.cuda.synchronize(device)
+
+        def capture(nsteps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(nsteps):
+                    step(i, i)
+            return g
+
+        self.reps, self.rem = divmod(steps, chunk)
+        self.g_main = capture(chunk) if self.reps else None
+        self.g_rem = capture(self.rem) if self.rem else None
+        for g in (self.g_main, self.g_rem):  # untimed: every captured step runs once
+            if g is not None:
+                g.replay()
+        torch.cuda.synchronize(device)
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def run(self, world, clocks_gpu):
+        """Times `steps` steps: barrier, synchronize, an L2 flush (a 512 MB write), then
+        the graph replays between two CUDA events on the launching stream."""
+        import torch
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(clocks_gpu) as clocks:
+            t_wall = time.time()
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize(self.device)
+            with torch.cuda.stream(self.stream):
+                self.flush.fill_(1)
+            start.record(self.stream)
+            for _ in range(self.reps):
+                self.g_main.replay()
+            if self.g_rem is not None:
+                self.g_rem.replay()
+            end.record(self.stream)
+            torch.cuda.synchronize(self.device)
+            if world > 1:
+                torch.distributed.barrier()
+            elapsed_ms = start.elapsed_time(end)
+            # keep the GPU busy (untimed) so that the clock sampler sees at least ~1.5 s of load
+            g = self.g_main or self.g_rem
+            while time.time() - t_wall < 1.5:
+                g.replay()
+                torch.cuda.synchronize(self.device)
+        return elapsed_ms, clocks.summary()
+
+    def bytes_per_launch(self):
+        """Mean algorithmic and dense bytes of the captured steps (outputs read back)."""
+        w, rows = self.w, self.w["per_step_rows"]
+        n = self.chunk if self.reps else self.rem
+        counts = self.out_c[:n].cpu().numpy()
+        alg, dense = [], []
+        for s in range(n):
+            r = (s % self.n_inputs) * rows
+            if self.tree:
+                sub = {k: (v[r:r + rows] if isinstance(v, np.ndarray) and v.shape[:1] == (w["target"].shape[0],)
+                           else v) for k, v in w.items()}
+                alg.append(algorithmic_bytes_tree(sub, counts[s], self.out_p[s].cpu().numpy()))
+                dense.append(dense_bytes_tree(sub))
+            else:
+                b = algorithmic_bytes_chain(w, range(r, r + rows), counts[s])
+                if self.sample:  # every draft row is read once more to draw the proposals
+                    b += rows * w["tokens"].shape[1] * w["draft"].shape[2] * w["draft"].dtype.itemsize
+                alg.append(b)
+                dense.append(dense_bytes_chain(w, range(r, r + rows)))
+        return float(np.mean(alg)), float(np.mean(dense)), float(counts.mean())
+
+
+
+def l2_note(w):
+    """How the timed region avoids L2 reuse of inputs, from the workload's shapes."""
+    rows = w["per_step_rows"]
+    n_inputs = w["target"].shape[0] // rows
+    set_mb = (w["target"].nbytes + w["draft"].nbytes) / n_inputs / 1e6
+    if n_inputs > 1:
+        return (f"L2 flushed ({L2_FLUSH_BYTES >> 20} MB write) right before the timed region; "
+                f"{n_inputs} resident input sets of {set_mb:.1f} MB cycled, so no set is read twice within "
+                f"{n_inputs * set_mb:.0f} MB of other inputs")
+    return (f"L2 flushed ({L2_FLUSH_BYTES >> 20} MB write) right before the timed region; one resident input set "
+            f"of {set_mb:.0f} MB, larger than L2, read every step")
+
+
+def roofline_entry(bytes_per_launch, dense_bytes, ms_per_step, traffic, prof, kernel):
+    peak, peak_src = measured_peak()
+    achieved = bytes_per_launch / (ms_per_step / 1e3) / 1e9
+    dense = dense_bytes / (ms_per_step / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (STREAM copy)",
+            "algorithmic_bytes_per_launch": bytes_per_launch,
+            "algorithmic_bytes": "rows the rule reads: target rows up to the first rejection (tree: the visited "
+                                 "nodes), the draft rows evaluated there, gathered draft entries, outputs",
+            "dense_bytes_per_launch": dense_bytes, "dense_achieved": dense, "dense_frac": dense / peak,
+            "dense_bytes": "every row of the call: all target rows, plus every draft-logit row of sampling rows "
+                           "(draft probabilities: the gathered entries and one row)",
+            "kernel": kernel, "traffic_source": prof}
+
+
+# workloads reported beside the headline in the default line: (key, make_workload name,
+# temperature); the large batch shares one set of logits across its temperatures
+SIDE_WORKLOADS = [("large_batch_T0.7", "large_batch", 0.7), ("large_batch_T0", "large_batch", 0.0),
+                  ("large_batch_T1.5", "large_batch", 1.5), ("mixed_batch", "mixed_batch", None),
+                  ("tree", "tree", None)]
+
+
+def run_side_workloads(args, rank, world, device, stream):
+    """The other verify workloads, each timed like the headline (same steps, warm-up, L2
+    flush) with its roofline and the oracle's bounded CPU baseline."""
+    import torch
+    from speculative_decoding_verification_53_gb300 import synth
+    out = {}
+    large, large_dev = None, None
+    gpu = device.index if device.index is not None else 0
+    for key, name, T in SIDE_WORKLOADS:
+        if name == "large_batch":
+            if large is None:
+                large = make_workload("large_batch", rank, args.rounds, 0, 0.7)
+                large_dev = {k: to_dev(large[k], device) for k in ("target", "draft")}
+            w = large if T == 0.7 else dict(synth.redraw_tokens(large, T, seed=100 + int(T * 10)),
+                                              desc=large["desc"].replace("T=0.7", f"T={T:g}"))
+            dev_inputs = large_dev
+        else:
+            w = make_workload(name, rank, args.rounds)
+            dev_inputs = None
+        t = Timed(w, device, stream, args.steps, args.warmup, dev_inputs=dev_inputs)
+        elapsed, clocks = t.run(world, gpu)
+        max_ms = slowest_rank_ms(elapsed, world, device)
+        ms = max_ms / args.steps
+        alg, dense, mean_count = t.bytes_per_launch()
+        traffic, prof, pk = profile_traffic(name, default_size=(name != "large_batch" or T == 0.7))
+        entry = {"workload": w["desc"], "ms_per_step": ms,
+                 "value": whole_job_rate(w["per_step_rows"], args.steps, world, max_ms),
+                 "unit": "trees/s" if w["kind"] == "tree" else UNIT, "mean_tokens_per_round": mean_count,
+                 "l2": l2_note(w), "clocks": clocks,
+                 "roofline": roofline_entry(alg, dense, ms, traffic, prof, pk or "kernel chosen by the library")}
+        if rank == 0 and not args.no_cpu_baseline:
+            entry["cpu_baseline"] = run_cpu_baseline(w, w["per_step_rows"], t.n_inputs, w["kind"] == "tree",
+                                                     budget_s=4.0)
+        out[key] = entry
+        del t
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, device):
     import torch
     import speculative_decoding_verification_53_gb300 as sv
@@ -279,118 +503,29 @@ def run_ours(args, rank, world, device):
     sv.lib()
     w = make_workload(args.workload, rank, args.rounds, args.batch, args.temperature)
     tree = w["kind"] == "tree"
-    rule = w.get("sibling_rule", "without_replacement")
-    sample = bool(w.get("sample"))
     per_step_rows = w["per_step_rows"]
     stream = torch.cuda.Stream(device)
     torch.cuda.set_stream(stream)
-
-    dt = to_dev(w["target"], device)
-    dd = to_dev(w["draft"], device)
-    if tree:
-        dtok, dpar = to_dev(w["node_tokens"], device), to_dev(w["parent"], device)
-    else:
-        dtok = to_dev(w["tokens"], device)
-    dtemp = to_dev(w["temperature"], device)
-    kind = "probs" if w["draft_kind"] == 0 else "logits"
-    n_inputs = dt.shape[0] // per_step_rows  # distinct resident input sets
-
-    chunk = min(args.steps, 1000)
-    K_ = w["tokens"].shape[1] if not tree else None
-    if tree:
-        D = w["max_depth"]
-        out_t = torch.empty((chunk, per_step_rows, D + 1), dtype=torch.int32, device=device)
-        out_c = torch.empty((chunk, per_step_rows), dtype=torch.int32, device=device)
-        out_p = torch.empty((chunk, per_step_rows, D), dtype=torch.int32, device=device)
-    else:
-        out_t = torch.empty((chunk, per_step_rows, K_ + 1), dtype=torch.int32, device=device)
-        out_c = torch.empty((chunk, per_step_rows), dtype=torch.int32, device=device)
-        out_x = torch.empty((chunk, per_step_rows, K_), dtype=torch.int32, device=device)
-
-    def step(i, slot):
-        r = (i % n_inputs) * per_step_rows
-        sl = slice(r, r + per_step_rows)
-        if tree:
-            sv.spec_verify_tree(dt[sl], dd[sl], dtok[sl], dpar[sl], dtemp[sl], D, 17, i, draft_kind=kind,
-                                out_tokens=out_t[slot], out_count=out_c[slot], out_path=out_p[slot],
-                                sibling_rule=rule)
-        elif sample:
-            sv.spec_sample_and_verify(dt[sl], dd[sl], dtemp[sl], 17, i, out_draft_tokens=out_x[slot],
-                                      out_tokens=out_t[slot], out_count=out_c[slot])
-        else:
-            sv.spec_verify_chain(dt[sl], dd[sl], dtok[sl], dtemp[sl], 17, i, draft_kind=kind,
-                                 out_tokens=out_t[slot], out_count=out_c[slot])
-
-    for i in range(max(args.warmup, 3)):
-        step(i, i % chunk)
-    torch.cuda.synchronize(device)
-
-    def capture(nsteps):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(nsteps):
-                step(i, i)
-        return g
-
-    reps, rem = divmod(args.steps, chunk)
-    g_main = capture(chunk) if reps else None
-    g_rem = capture(rem) if rem else None
-    for g in (g_main, g_rem):
-        if g is not None:
-            g.replay()
-    torch.cuda.synchronize(device)
-
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(device.index if device.index is not None else 0) as clocks:
-        t_wall = time.time()
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize(device)
-        start.record(stream)
-        for _ in range(reps):
-            g_main.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        end.record(stream)
-        torch.cuda.synchronize(device)
-        if world > 1:
-            torch.distributed.barrier()
-        elapsed_ms = start.elapsed_time(end)
-        # keep the GPU busy (untimed) so that the clock sampler sees at least ~1.5 s of load
-        while time.time() - t_wall < 1.5 and g_main is not None:
-            g_main.replay()
-            torch.cuda.synchronize(device)
-    clock = clocks.summary()
-
-    # per-step algorithmic bytes of the captured steps (read back their outputs)
-    steps_in_chunk = chunk if reps else rem
-    counts = out_c[:steps_in_chunk].cpu().numpy()
-    if tree:
-        paths = out_p[:steps_in_chunk].cpu().numpy()
-        bytes_steps = [algorithmic_bytes_tree(w, counts[s], paths[s]) for s in range(steps_in_chunk)]
-    else:
-        bytes_steps = []
-        for s in range(steps_in_chunk):
-            r = (s % n_inputs) * per_step_rows
-            b = algorithmic_bytes_chain(w, range(r, r + per_step_rows), counts[s])
-            if sample:  # every draft row is read once more to draw the proposals
-                b += per_step_rows * K_ * w["draft"].shape[2] * w["draft"].dtype.itemsize
-            bytes_steps.append(b)
-    bytes_per_launch = float(np.mean(bytes_steps))
-    mean_count = float(counts.mean())
+    t = Timed(w, device, stream, args.steps, args.warmup)
+    elapsed_ms, clock = t.run(world, device.index if device.index is not None else 0)
+    bytes_per_launch, dense_bytes, mean_count = t.bytes_per_launch()
+    n_inputs, resident = t.n_inputs, t.resident_bytes
+    del t
 
     max_ms = slowest_rank_ms(elapsed_ms, world, device)
     ms_per_step = max_ms / args.steps
     value = whole_job_rate(per_step_rows, args.steps, world, max_ms)
 
     # end to end: host buffers, copies inside the timed region, through the public API
+    kind = "probs" if w["draft_kind"] == 0 else "logits"
     e2e = run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind)
 
     cpu = run_cpu_baseline(w, per_step_rows, n_inputs, tree) if (rank == 0 and not args.no_cpu_baseline) else None
+    side = None
+    if args.workload == "single_stream" and not args.no_side_workloads:
+        side = run_side_workloads(args, rank, world, device, stream)
     if rank != 0:
         return None
-    peak, peak_src = measured_peak()
-    achieved = bytes_per_launch / (ms_per_step / 1e3) / 1e9
     traffic, prof, prof_kernel = profile_traffic(args.workload, default_size=not (args.batch or args.temperature is not None
                                                                                or args.rounds != 64))
     line = {
@@ -406,23 +541,28 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w["desc"], "batch_rows_per_step": per_step_rows,
-                   "resident_input_sets": n_inputs,
-                   "resident_bytes": int(dt.numel() * dt.element_size() + dd.numel() * dd.element_size()),
-                   "l2": "inputs larger than L2 (resident sets cycled, no flush)",
-                   "timing": "CUDA-graph replay, CUDA events on the launching stream",
-                   "parallelism": f"replicas x{world}", "mean_tokens_per_round": mean_count},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (STREAM copy)",
-                     "algorithmic_bytes_per_launch": bytes_per_launch,
-                     "kernel": prof_kernel or ("tree_kernel" if tree else "chain kernel chosen by the library"),
-                     "traffic_source": prof},
+        "config": workload_config(w, world),
+        "resident_input_sets": n_inputs,
+        "resident_bytes": resident,
+        "mean_tokens_per_round": mean_count,
+        "roofline": roofline_entry(bytes_per_launch, dense_bytes, ms_per_step, traffic, prof,
+                                   prof_kernel or ("tree_kernel" if tree else "chain kernel chosen by the library")),
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": args.steps * (2 if w.get("sample") else 1),  # sampling + verify kernels per step
         "clocks": clock,
     }
+    if side is not None:
+        line["workloads"] = side
     return line
+
+
+def workload_config(w, world):
+    """The `config` object of both arms: the workload, its batch rows per step, how it
+    is timed and how it is parallelised."""
+    return {"workload": w["desc"], "batch_rows_per_step": w["per_step_rows"], "l2": l2_note(w),
+            "timing": "CUDA-graph replay, CUDA events on the launching stream",
+            "parallelism": f"replicas x{world}"}
 
 
 def _packed(arrays, device):
@@ -584,8 +724,7 @@ def run_reference(args, rank):
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": done,
             "warmup": max(args.warmup, 3), "ms_per_step": el / max(done, 1) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": w["desc"], "batch_rows_per_step": per_step_rows,
-                       "steps_requested": args.steps, "time_budget_s": budget},
+            "config": workload_config(w, args.gpus), "steps_requested": args.steps, "time_budget_s": budget,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{done} steps of the workload on one host core (fp64 C oracle)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -605,9 +744,18 @@ def make_aux(args, rank):
         N = args.nodes or 1024
         par = synth.random_parents(seed, B, N, shape="bfs", branch=3, max_depth=6 if N <= 64 else 16)
         W = (N + 31) // 32
+        bytes_per_step = B * N * 4 + B * N * W * 4 + B * N * 4 + B * 4
+        # distinct parent and output buffers per step, cycled, so that the bytes touched
+        # between two uses of one buffer exceed twice the L2 (129 MB)
+        n_sets = max(2, -(-2 * (129 << 20) // bytes_per_step))
+        chunk = min(args.steps, 1000)
+        n_graphs = -(-n_sets // chunk) if n_sets > chunk else 1
+        n_sets = n_graphs * chunk if n_sets > chunk else n_sets
         return dict(parent=par, B=B, N=N, W=W, metric=f"tree-attention masks/s (N={N}-node draft trees)",
-                    unit="trees/s", per_step=B,
-                    bytes_per_step=B * N * 4 + B * N * W * 4 + B * N * 4 + B * 4,
+                    unit="trees/s", per_step=B, n_sets=n_sets, n_graphs=n_graphs,
+                    l2="%d distinct parent/output sets cycled (%.0f MB between reuses, larger than L2)" % (
+                        n_sets, n_sets * bytes_per_step / 1e6),
+                    bytes_per_step=bytes_per_step,
                     desc=f"tree-attention mask, B={B} trees of N={N} nodes (breadth-first, up to 3 children, "
                          f"depth<={6 if N <= 64 else 16}), uint32 ancestor bitmask [B][N][{W}] + depth")
     L = dict(KV_LAYOUT)
@@ -619,11 +767,18 @@ def make_aux(args, rank):
     row_bytes = L["dim"] * 2
     per_set = moves.reshape(L["sets"], B).sum(1) * 2 * row_bytes * L["heads"] * L["n_buffers"]
     return dict(path=path, count=count, base=base, B=B, layout=L, per_step=B,
+                l2=f"{L['sets']} path sets in disjoint cache windows cycled (touched bytes per cycle > L2)",
                 metric="accepted-path KV compactions/s (batch rows, every layer's K and V)", unit="batch rows/s",
                 bytes_per_set=per_set, row_bytes=row_bytes,
                 desc=f"accepted-path KV compaction, B={B}, {L['n_buffers']} cache tensors (32 layers x K,V) of "
                      f"[B][{L['heads']} heads][{L['rows']} rows][{L['dim']}] bf16, tree of {L['nodes']} nodes, "
                      f"depth<={L['depth']}, {L['sets']} resident path sets in disjoint row windows")
+
+
+def aux_config(a, world):
+    """The `config` object of both arms for the steps around a tree verify."""
+    return {"workload": a["desc"], "batch_rows_per_step": a["per_step"], "l2": a["l2"],
+            "timing": "CUDA-graph replay, CUDA events on the launching stream", "parallelism": f"replicas x{world}"}
 
 
 def run_aux(args, rank, world, device):
@@ -641,13 +796,7 @@ def run_aux(args, rank, world, device):
     chunk = min(args.steps, 1000)
     n_graphs = 1
     if args.workload == "tree_mask":
-        # Distinct parent and output buffers per step, cycled, so that the bytes touched
-        # between two uses of one buffer exceed twice the L2.
-        l2_bytes = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (129 << 20)
-        n_sets = max(2, -(-2 * l2_bytes // a["bytes_per_step"]))
-        if n_sets > chunk:
-            n_graphs = -(-n_sets // chunk)
-            n_sets = n_graphs * chunk
+        n_sets, n_graphs = a["n_sets"], a["n_graphs"]
         dpar = torch.from_numpy(a["parent"]).to(device).unsqueeze(0).repeat(n_sets, 1, 1)
         om = torch.empty((n_sets, a["B"], a["N"], a["W"]), dtype=torch.int32, device=device)
         od = torch.empty((n_sets, a["B"], a["N"]), dtype=torch.int32, device=device)
@@ -659,8 +808,6 @@ def run_aux(args, rank, world, device):
 
         def bytes_of(i):
             return a["bytes_per_step"]
-        l2 = "%d distinct parent/output sets cycled (%.0f MB between reuses, larger than L2)" % (
-            n_sets, n_sets * a["bytes_per_step"] / 1e6)
         kernel = "tree_mask_kernel"
     else:
         L = a["layout"]
@@ -681,7 +828,6 @@ def run_aux(args, rank, world, device):
 
         def bytes_of(i):
             return float(a["bytes_per_set"][i % L["sets"]])
-        l2 = f"{L['sets']} path sets in disjoint cache windows cycled (touched bytes per cycle > L2)"
         kernel = "kv_compact_kernel"
 
     for i in range(max(args.warmup, 3)):
@@ -734,9 +880,7 @@ def run_aux(args, rank, world, device):
         "metric": a["metric"], "value": value, "unit": a["unit"], "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u32" if args.workload == "tree_mask" else "u8", "data": "synthetic",
-        "config": {"workload": a["desc"], "batch_rows_per_step": a["per_step"], "l2": l2,
-                   "timing": "CUDA-graph replay, CUDA events on the launching stream",
-                   "parallelism": f"replicas x{world}"},
+        "config": aux_config(a, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (STREAM copy)",
                      "algorithmic_bytes_per_launch": bytes_per_launch, "kernel": prof_kernel or kernel,
@@ -842,8 +986,7 @@ def run_aux_reference(args, rank):
             "warmup": max(args.warmup, 3), "ms_per_step": el / max(steps, 1) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u32" if args.workload == "tree_mask" else "u8",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": a["desc"], "batch_rows_per_step": a["per_step"], "steps_requested": args.steps,
-                       "time_budget_s": 120.0},
+            "config": aux_config(a, args.gpus), "steps_requested": args.steps, "time_budget_s": 120.0,
             "cpu_baseline": {"value": value, "unit": a["unit"], "cores": 1, "kind": "oracle",
                              "sample": f"{sample} on one host core (C oracle)"},
             "e2e": {"value": value, "unit": a["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -867,6 +1010,8 @@ def main():
     ap.add_argument("--nodes", type=int, default=0, help="tree nodes of the tree_mask workload (default 1024)")
     ap.add_argument("--temperature", type=float, default=None, help="temperature of the large-batch workload")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-side-workloads", action="store_true",
+                    help="default workload only: skip the large-batch, mixed-batch and tree entries of `workloads`")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -29,3 +29,24 @@ def test_reference_arm_prints_the_contract_line(extra, unit):
     assert e2e["value"] == line["value"] and e2e["unit"] == unit
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     assert "workload" in line["config"]
+
+
+def test_both_arms_print_the_same_config():
+    """The reference arm's `config` is the one the GPU arm prints for the same workload
+    (both come from one function of the workload), so the driver can compare the arms."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
+                          "--workload", "single_stream", "--rounds", "2"], cwd=ROOT, capture_output=True, text=True,
+                         timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["config"] == bench.workload_config(bench.make_workload("single_stream", 0, 2), 1)
+    args = argparse.Namespace(workload="tree_mask", batch=8, nodes=60, steps=1)
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
+                          "--workload", "tree_mask", "--batch", "8", "--nodes", "60"], cwd=ROOT, capture_output=True,
+                         text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["config"] == bench.aux_config(bench.make_aux(args, 0), 1)
