@@ -49,6 +49,13 @@
  *    draft probability at a drafted token is negative or not finite, or whose
  *    parent array is malformed, gets out_count[b] = 0 and all output slots -1.
  *    A valid row always has out_count[b] >= 1.
+ *  - Every device-side wait (for a bulk copy, or for the partial results the CTAs of
+ *    a thread-block cluster exchange) is bounded to a quarter of a second.  A wait
+ *    that gives up does not fail the call either: the walking chain and tree kernels
+ *    give that row out_count[b] = -1 (its other outputs are then unspecified), and
+ *    spec_verify_rows_status turns it into the call's SV_ERR_TIMEOUT.  The
+ *    position-parallel small-batch chain kernel reports such a row as invalid data
+ *    (out_count[b] = 0): its per-row word has no room for a third state.
  *  - Calls that share a workspace must not overlap on the GPU.
  */
 #ifndef SPEC_VERIFY_H
@@ -72,7 +79,8 @@ typedef enum {
     SV_ERR_INVALID_ARG = 1, /* a size, pointer, dtype or kind argument is invalid */
     SV_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles (size limits, device) */
     SV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-    SV_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up; the workspace must be re-zeroed */
+    SV_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up on some row (out_count = -1, see
+                               spec_verify_rows_status); re-zero the workspace before reusing it */
     SV_ERR_BAD_INPUT = 5    /* some batch rows held invalid data (see spec_verify_count_invalid) */
 } sv_status;
 
@@ -102,7 +110,7 @@ SV_API size_t spec_verify_workspace_size(int B, int K, int V);
  *   out_tokens     device int32 [B][K+1]: accepted drafts, then the replacement or
  *                  bonus token; unused slots are -1.
  *   out_count      device int32 [B]: number of valid entries in out_tokens[b]
- *                  (1..K+1; 0 for an invalid row).
+ *                  (1..K+1; 0 for an invalid row; -1 where a bounded wait gave up).
  *   out_accept_prob  nullable device fp32 [B][K]: min(1, p_k(x_k)/q_k(x_k)) for every
  *                  position up to and including the first rejection (greedy rows:
  *                  1 for a match, 0 for the mismatch); -1 for positions never
@@ -126,12 +134,13 @@ SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt,
  * code running inside a runtime that owns every device allocation (an engine's
  * memory arena, a plugin interface that passes only input and output buffers) or a
  * path on which no allocation call is allowed.  Same arguments and outputs as
- * spec_verify_chain, minus the workspace.  Where it applies (small batches, aligned
- * rows) it runs the position-parallel kernel, whose scratch is a 256 KiB array inside
- * the library's device image, present on every device that loads the library until
- * the process exits; otherwise it runs the kernels that need no scratch.  Results
- * agree with spec_verify_chain except where a decision lies within fp32 rounding of
- * its boundary.  No cudaMalloc, cudaFree or other allocating call is made.
+ * spec_verify_chain, minus the workspace, and the same kernel choice: where
+ * spec_verify_chain would run the position-parallel kernel (small and moderate
+ * batches, aligned rows) this entry runs it too, with its scratch in a 256 KiB array
+ * inside the library's device image, present on every device that loads the library
+ * until the process exits; elsewhere it runs the kernels that need no scratch.
+ * Results agree with spec_verify_chain except where a decision lies within fp32
+ * rounding of its boundary.  No cudaMalloc, cudaFree or other allocating call is made.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress, with the device current) and zeroes it synchronously;
  *     make that first call before any stream capture.
@@ -258,6 +267,22 @@ SV_API const char *spec_verify_last_cuda_error(void);
  * range, out_invalid NULL, out_count NULL with B > 0), SV_ERR_CUDA (launch failure).
  */
 SV_API sv_status spec_verify_count_invalid(const int32_t *out_count, int B, int32_t *out_invalid, void *stream);
+
+/*
+ * Row status of a finished verify call (the pages have no counterpart: this reports
+ * device-side failures).  Rows with out_count[b] = -1 are rows on which a bounded
+ * device-side wait gave up; rows with out_count[b] = 0 hold invalid data.
+ * Writes, on the device and in stream order after the call:
+ *   out_status[0]  the call's status: SV_ERR_TIMEOUT if any row has count -1, else
+ *                  SV_ERR_BAD_INPUT if any row has count 0, else SV_OK;
+ *   out_status[1]  the number of rows with count 0;
+ *   out_status[2]  the number of rows with count -1.
+ *   out_count    device int32 [B], as any verify entry writes it; 0 <= B <= 1<<24.
+ *   out_status   device int32 [3], written once (no initialisation needed).
+ * One kernel on `stream`; nothing is allocated.  Errors: SV_ERR_INVALID_ARG (B out of
+ * range, out_status NULL, out_count NULL with B > 0), SV_ERR_CUDA (launch failure).
+ */
+SV_API sv_status spec_verify_rows_status(const int32_t *out_count, int B, int32_t *out_status, void *stream);
 
 #ifdef __cplusplus
 }

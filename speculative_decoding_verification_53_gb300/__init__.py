@@ -26,7 +26,10 @@ SV_SIBLINGS_WITHOUT_REPLACEMENT, SV_SIBLINGS_IID = 0, 1
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_chain", "spec_greedy_accept", "spec_verify_tree",
            "spec_verify_status_string", "spec_verify_last_cuda_error", "spec_verify_chain_noalloc",
            "spec_tree_mask", "spec_kv_compact", "spec_verify_tree_rule", "spec_sample_and_verify",
-           "spec_verify_count_invalid")
+           "spec_verify_count_invalid", "spec_verify_rows_status")
+
+# out_count value of a batch row whose kernel gave up a bounded device-side wait
+COUNT_TIMEOUT = -1
 
 _lib = None
 
@@ -76,6 +79,8 @@ def lib() -> ctypes.CDLL:
     L.spec_verify_last_cuda_error.restype = ctypes.c_char_p
     L.spec_verify_count_invalid.argtypes = [vp, ci, vp, vp]
     L.spec_verify_count_invalid.restype = ci
+    L.spec_verify_rows_status.argtypes = [vp, ci, vp, vp]
+    L.spec_verify_rows_status.restype = ci
     _lib = L
     return L
 
@@ -330,12 +335,29 @@ def spec_verify_count_invalid(out_count, *, out_invalid=None, stream=None):
     return out_invalid
 
 
+def spec_verify_rows_status(out_count, *, out_status=None, stream=None):
+    """Row-status summary of a finished verify call, computed on the device in stream
+    order: an int32 device tensor [3] = (the call's sv_status -- SV_ERR_TIMEOUT if a row
+    has count -1, else SV_ERR_BAD_INPUT if a row has count 0, else SV_OK --, the rows
+    with count 0, the rows with count -1)."""
+    torch = _torch()
+    _dev(out_count, "out_count", torch.int32)
+    if out_status is None:
+        out_status = torch.empty((3,), dtype=torch.int32, device=out_count.device)
+    st = lib().spec_verify_rows_status(_ptr(out_count), out_count.numel(), _ptr(out_status), _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_rows_status")
+    return out_status
+
+
 def rows_status(out_count, *, stream=None) -> int:
-    """SV_ERR_BAD_INPUT if any batch row of a finished verify call is invalid, else
-    SV_OK (reads one int32 back, so it waits for the stream)."""
-    n = spec_verify_count_invalid(out_count, stream=stream)
+    """The sv_status of a finished verify call's rows: SV_ERR_TIMEOUT if a bounded
+    device-side wait gave up on some row (count -1), SV_ERR_BAD_INPUT if some row held
+    invalid data (count 0), else SV_OK.  Reads three int32 back, so it waits for the
+    stream."""
+    s = spec_verify_rows_status(out_count, stream=stream)
     (_torch().cuda.current_stream() if stream is None else stream).synchronize()
-    return SV_ERR_BAD_INPUT if int(n.cpu().item()) > 0 else SV_OK
+    return int(s[0].cpu().item())
 
 
 def spec_tree_mask(parent, *, out_mask=None, out_depth=None, out_valid=None, stream=None):

@@ -32,12 +32,11 @@ constexpr int kMaxB = 65535;
 
 // Launch-shape override for tuning: SPEC_VERIFY_CLUSTER in {1, 2, 4, 8, 16}.
 int cluster_override() {
-    static int v = -1;
-    if (v < 0) {
+    static const int v = [] {  // read once (thread-safe initialisation)
         const char* s = std::getenv("SPEC_VERIFY_CLUSTER");
-        int x = s ? std::atoi(s) : 0;
-        v = (x == 1 || x == 2 || x == 4 || x == 8 || x == 16) ? x : 0;
-    }
+        const int x = s ? std::atoi(s) : 0;
+        return (x == 1 || x == 2 || x == 4 || x == 8 || x == 16) ? x : 0;
+    }();
     return v;
 }
 
@@ -62,22 +61,36 @@ sv_status device_info(DeviceInfo& info) {
 
 // Kernel-family override for comparison runs and tests: SPEC_VERIFY_PATH =
 // "spec" (position-parallel), "staged" (shared-memory staging), "stream"
-// (register streaming); anything else picks automatically.
-enum PathChoice { PATH_AUTO = 0, PATH_SPEC = 1, PATH_STAGED = 2, PATH_STREAM = 3, PATH_EAGER = 4 };
+// (register streaming), "eager" (all positions staged at once), "ring" (ring-streamed
+// walk); anything else picks automatically.
+enum PathChoice { PATH_AUTO = 0, PATH_SPEC = 1, PATH_STAGED = 2, PATH_STREAM = 3, PATH_EAGER = 4, PATH_RING = 5 };
 
 int path_override() {
-    static int v = -1;
-    if (v < 0) {
+    static const int v = [] {  // read once (thread-safe initialisation)
         const char* s = std::getenv("SPEC_VERIFY_PATH");
-        v = PATH_AUTO;
+        int r = PATH_AUTO;
         if (s) {
             const std::string p(s);
-            if (p == "spec") v = PATH_SPEC;
-            if (p == "staged") v = PATH_STAGED;
-            if (p == "stream") v = PATH_STREAM;
-            if (p == "eager") v = PATH_EAGER;
+            if (p == "spec") r = PATH_SPEC;
+            if (p == "staged") r = PATH_STAGED;
+            if (p == "stream") r = PATH_STREAM;
+            if (p == "eager") r = PATH_EAGER;
+            if (p == "ring") r = PATH_RING;
         }
-    }
+        return r;
+    }();
+    return v;
+}
+
+// Test hook for the timeout path (SPEC_VERIFY_TEST_STALL=<row>): in the shared-memory
+// staged walk, batch row <row> announces its first copy without issuing it, so its
+// bounded wait runs out after 50 us and the row reports out_count = -1.  Off (-1) unless
+// the variable is set; read once.
+int stall_row_override() {
+    static const int v = [] {
+        const char* s = std::getenv("SPEC_VERIFY_TEST_STALL");
+        return s ? std::atoi(s) : -1;
+    }();
     return v;
 }
 
@@ -91,16 +104,21 @@ size_t round16(size_t x) { return (x + 15) & ~(size_t)15; }
 // (rows not 16-byte aligned, or one slot does not fit in shared memory).
 sv::StageLayout chain_stage_layout(const void* target, int tdt, const void* draft, int ddt, int dk, bool uses_draft,
                                    int B, int K, int V, int G, int num_sms) {
-    sv::StageLayout L{0, 0, 0, 0, 0};
+    sv::StageLayout L{0, 0, 0, 0, 0, 0};
     const size_t tsz = dtype_size(tdt), dsz = dk == SV_DRAFT_PROBS ? 4 : dtype_size(ddt);
     if (!aligned16(target) || (V * tsz) % 16) return L;
     if (uses_draft && (!aligned16(draft) || (V * dsz) % 16)) return L;
     const size_t nvec = (V + 7) / 8, cmax = ((nvec + G - 1) / G) * 8;
     const size_t t_bytes = round16(cmax * tsz);
-    const size_t d_bytes = (uses_draft && dk == SV_DRAFT_LOGITS) ? round16(cmax * dsz) : 0;
+    const bool small = (long long)B * G <= num_sms;  // one CTA per SM or fewer: prefetch positions ahead
+    // Large batches keep only the target chunk on chip and stream the draft-logit row from
+    // global memory (its statistics while the target chunk lands, its second read for the
+    // draw from L2): half the shared memory per row, so twice the rows in flight.
+    // Measured at B = 256, K = 8, V = 152064, T = 0.7 (clusters of 8): see the kernel.
+    const bool d_direct = !small && uses_draft && dk == SV_DRAFT_LOGITS;
+    const size_t d_bytes = (uses_draft && dk == SV_DRAFT_LOGITS && !d_direct) ? round16(cmax * dsz) : 0;
     const size_t probs = (uses_draft && dk == SV_DRAFT_PROBS) ? round16(cmax * 4) : 0;
     const size_t fixed = sv::STAGE_HEADER + probs + sv::draw_smem_bytes(V, G) + 64;
-    const bool small = (long long)B * G <= num_sms;  // one CTA per SM or fewer: prefetch positions ahead
     const size_t budget = small ? (size_t)sv::MAX_DYN_SMEM - 8192 : (size_t)100 * 1024;
     const size_t slot = t_bytes + d_bytes;
     if (fixed + slot > budget) return L;
@@ -112,6 +130,7 @@ sv::StageLayout chain_stage_layout(const void* target, int tdt, const void* draf
     L.t_bytes = (int)t_bytes;
     L.probs_bytes = (int)probs;
     L.prefetch_l2 = small ? 1 : 0;
+    L.d_direct = d_direct ? 1 : 0;
     return L;
 }
 
@@ -142,11 +161,41 @@ int spec_cluster(int B, int K, int V, int tsz, int dsz, int num_sms, bool forced
     return forced ? G : 0;
 }
 
+// Cluster size of the ring-streamed walk (sv_chain_ring.cu), or 0 where it is not the
+// kernel to take.  It is made for batches too large to stage on chip: clusters of 4
+// CTAs of 128 threads (each CTA at least one full 2048-element stage of the row), taken
+// when B clusters fill the SMs at least twice over, so that every row is resident
+// while HBM streams.  forced (SPEC_VERIFY_PATH=ring): any batch, a cluster of 4, or of
+// SPEC_VERIFY_CLUSTER (2, 4 or 8) when set.
+int ring_cluster(int B, int V, int num_sms, bool forced) {
+    int G = 4;
+    const int o = cluster_override();
+    if (forced && (o == 1 || o == 2 || o == 4 || o == 8)) G = o;
+    if (forced) {
+        while (G > 1 && V < G * 8) G >>= 1;  // every CTA owns part of the row
+        return G;
+    }
+    (void)B;
+    (void)num_sms;
+    return 0;  // measured slower than the staged walk on every batch tried (only when forced)
+}
+
+// Stage layout of the ring-streamed walk: three stages of 2048 elements of the target
+// row and of the draft row (logits, or fp32 probabilities for the draw).
+sv::RingLayout chain_ring_layout(int tdt, int ddt, int dk, bool uses_draft) {
+    sv::RingLayout R{3, 0, 0};
+    R.t_bytes = (int)round16((size_t)2048 * dtype_size(tdt));
+    const size_t d = uses_draft ? round16((size_t)2048 * (dk == SV_DRAFT_PROBS ? 4 : dtype_size(ddt))) : 0;
+    R.stage_bytes = R.t_bytes + (int)d;
+    return R;
+}
+
 // Kernel choice for a chain launch:
 //  - position-parallel (sv_chain_spec.cu) for small and moderate batches when a workspace
 //    is given (spec_cluster): every position of every row at once, the latency of one
 //    position instead of K+1, at the price of reading the positions after the first
 //    rejection;
+//  - ring-streamed walk (sv_chain_ring.cu) for large batches of aligned rows (ring_cluster);
 //  - shared-memory staged walk (sv_chain_staged.cu) when rows are 16-byte aligned;
 //  - register-streaming walk (sv_chain.cu) otherwise.
 sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_draft, int num_sms, void* ws,
@@ -177,10 +226,23 @@ sv_status run_chain(const sv::ChainArgs& a, int tdt, int ddt, int dk, bool uses_
             (void)cudaGetLastError();
         }
     }
+    if ((path == PATH_AUTO || path == PATH_RING) && aligned) {
+        const int Gr = ring_cluster(a.B, a.V, num_sms, path == PATH_RING);
+        if (Gr > 0) {
+            const cudaError_t e =
+                sv::launch_chain_ring(a, chain_ring_layout(tdt, ddt, dk, uses_draft), tdt, ddt, dk, Gr, stream);
+            if (e == cudaSuccess) return SV_OK;
+            if (e != cudaErrorInvalidClusterSize) return launch_status(e);
+            (void)cudaGetLastError();
+        }
+    }
     const int G = sv::choose_cluster(a.B, a.V, num_sms);
     const sv::StageLayout L = chain_stage_layout(a.target, tdt, a.draft, ddt, dk, uses_draft, a.B, a.K, a.V, G, num_sms);
     if (L.nslot > 0 && path != PATH_STREAM) {
-        const cudaError_t e = sv::launch_chain_staged(a, L, tdt, ddt, dk, G, stream);
+        sv::ChainArgs as = a;
+        as.stall_row = stall_row_override();
+        as.stall_ns = 50000u;
+        const cudaError_t e = sv::launch_chain_staged(as, L, tdt, ddt, dk, G, stream);
         if (e == cudaSuccess) return SV_OK;
         if (e != cudaErrorInvalidClusterSize) return launch_status(e);
         (void)cudaGetLastError();
@@ -197,8 +259,9 @@ sv_status chain_with_scratch(const void* target_logits, int tdt, const void* dra
                              const int32_t* draft_tokens, const float* temperature, int B, int K, int V,
                              uint64_t seed, uint64_t offset, int32_t* out_tokens, int32_t* out_count,
                              float* out_accept_prob, void* scratch, size_t scratch_bytes, void* stream) {
-    // same checks as spec_verify_chain; the position-parallel kernel (the one that uses the
-    // scratch) is taken whenever it applies, the scratch-free kernels otherwise
+    // same checks and the same kernel choice as spec_verify_chain, with the scratch as
+    // the workspace: the position-parallel kernel (the one that uses it) where the
+    // automatic rule picks it, the kernels that need no scratch elsewhere
     if (B < 0 || B > kMaxB || K < 0 || K > kMaxK || V < 1 || V > kMaxV) return SV_ERR_INVALID_ARG;
     if (!is_dtype(tdt) || !is_dtype(ddt)) return SV_ERR_INVALID_ARG;
     if (dk != SV_DRAFT_PROBS && dk != SV_DRAFT_LOGITS) return SV_ERR_INVALID_ARG;
@@ -211,7 +274,7 @@ sv_status chain_with_scratch(const void* target_logits, int tdt, const void* dra
     if (st != SV_OK) return st;
     ChainArgs a{target_logits, draft, draft_tokens, temperature, B, K, V, seed, offset,
                 out_tokens, out_count, out_accept_prob};
-    return run_chain(a, tdt, ddt, dk, K > 0, info.sms, scratch, scratch_bytes, (cudaStream_t)stream, PATH_SPEC);
+    return run_chain(a, tdt, ddt, dk, K > 0, info.sms, scratch, scratch_bytes, (cudaStream_t)stream);
 }
 
 int choose_cluster(int B, int V, int num_sms) {
@@ -333,7 +396,7 @@ sv_status spec_verify_tree_rule(const void* target_logits, sv_dtype tdt, const v
     if (path_override() != PATH_STREAM && aligned16(target_logits) && aligned16(draft) && (V * tsz) % 16 == 0 &&
         (V * dsz) % 16 == 0) {
         const size_t nvec = (V + 7) / 8, cmax = ((nvec + G - 1) / G) * 8;
-        sv::StageLayout L{0, 0, 0, 0, 0};
+        sv::StageLayout L{0, 0, 0, 0, 0, 0};
         L.t_bytes = (int)round16(cmax * tsz);
         L.slot_bytes = L.t_bytes + (int)round16(cmax * dsz);
         const bool small = (long long)B * G <= info.sms;

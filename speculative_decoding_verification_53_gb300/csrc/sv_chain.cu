@@ -88,13 +88,15 @@ __global__ void __launch_bounds__(NT) chain_kernel(const ChainArgs a) {
         for (int k = threadIdx.x; k <= K; k += NT) slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)k, s_r[k], s_u[k]);
     bool invalid = __syncthreads_or(tok_bad) != 0;
 
-    int phase = 0, j = -1, final_tok = -1, writer = 0;
+    // tmo: some wait of the row gave up (this CTA's, or a peer's flag seen in an exchange)
+    int phase = 0, j = -1, final_tok = -1, writer = 0, tmo = 0;
     for (int k = 0; k <= K && !invalid; ++k) {
         const void* trow = (const char*)a.target + ((size_t)b * (K + 1) + k) * (size_t)V * tsz;
         const bool at = ((uintptr_t)trow & 15) == 0;
         if (greedy) {
             ArgMax am = thread_argmax<TDT>(trow, lo, hi, at);
             am = cluster_argmax(am, sc, phase);
+            if (am.bad & BAD_TIMEOUT) tmo = 1;
             if (am.bad || !(am.v > neg_inf()) || am.v == pos_inf()) { invalid = true; break; }
             if (k < K && s_tok[k] == am.i) {
                 if (threadIdx.x == 0) s_ap[k] = 1.f;
@@ -112,11 +114,13 @@ __global__ void __launch_bounds__(NT) chain_kernel(const ChainArgs a) {
         LSE ds{neg_inf(), 0.f, 0};
         if (DK == DK_LOGITS && k < K) ds = thread_lse<DDT>(drow, lo, hi, ad, c);
         cluster_lse2(ts, ds, c, sc, phase);
+        if ((ts.bad | ds.bad) & BAD_TIMEOUT) tmo = 1;
         if (row_bad(ts) || (DK == DK_LOGITS && k < K && row_bad(ds))) { invalid = true; break; }
         const float inv_st = 1.f / ts.s;
         if (k == K) {  // every draft accepted: bonus token from p_K
             const PWeights<TDT> pw{trow, c, ts.m, inv_st, at};
             const DrawResult d = cluster_draw(pw, lo, hi, s_u[K], tile_sum, sc, phase);
+            if (d.failed) { tmo = 1; invalid = true; break; }
             j = K;
             final_tok = d.token;
             writer = d.owner;
@@ -138,9 +142,11 @@ __global__ void __launch_bounds__(NT) chain_kernel(const ChainArgs a) {
         // first rejection: replacement from the residual (p_k - q_k)+
         const ResidualWeights<TDT, DDT, DK> rw{trow, drow, c, ts.m, inv_st, ds.m, inv_sd, at, ad};
         DrawResult d = cluster_draw(rw, lo, hi, s_u[k], tile_sum, sc, phase);
+        if (d.failed) { tmo = 1; invalid = true; break; }
         if (d.owner < 0) {  // the residual has no mass: draw from p_k
             const PWeights<TDT> pw{trow, c, ts.m, inv_st, at};
             d = cluster_draw(pw, lo, hi, s_u[k], tile_sum, sc, phase);
+            if (d.failed) { tmo = 1; invalid = true; break; }
         }
         j = k;
         final_tok = d.token;
@@ -155,11 +161,15 @@ __global__ void __launch_bounds__(NT) chain_kernel(const ChainArgs a) {
             ot[i] = invalid ? -1 : (i < j ? s_tok[i] : (i == j ? final_tok : -1));
         if (a.out_accept_prob)
             for (int i = threadIdx.x; i < K; i += NT) a.out_accept_prob[(size_t)b * K + i] = invalid ? -1.f : s_ap[i];
-        if (threadIdx.x == 0) a.out_count[b] = invalid ? 0 : j + 1;
+        if (threadIdx.x == 0) a.out_count[b] = invalid ? (tmo ? SV_COUNT_TIMEOUT : 0) : j + 1;
     }
-    // No trailing cluster barrier: peers only ever push into this CTA's inbox, and the
-    // last exchange (the same sequence in every CTA of the cluster) completed on this
-    // CTA's own barrier, so nothing is written into its shared memory any more.
+    // Leave together: when every exchange completes, the walk is the same in every CTA of
+    // the cluster and nothing is pushed into a CTA after its last exchange; but a CTA
+    // whose bounded wait gave up may have left the walk early while a peer still pushes
+    // into its inbox.  Every wait before this barrier is bounded, so every CTA reaches
+    // it.  A CTA that saw a timeout then marks the row (after any other writer).
+    cluster_sync_all();
+    if (tmo && threadIdx.x == 0) a.out_count[b] = SV_COUNT_TIMEOUT;
 }
 
 size_t draw_smem_bytes(int V, int cluster) {
@@ -171,24 +181,15 @@ size_t draw_smem_bytes(int V, int cluster) {
 template <int TDT, int DDT, int DK>
 static cudaError_t launch_chain_t(const ChainArgs& a, int G, cudaStream_t stream) {
     auto kern = chain_kernel<TDT, DDT, DK>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    static int max_cluster = 0;  // largest cluster the device co-schedules for this kernel
+    static KernelLaunchCache cache;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.stream = stream;
-    if (max_cluster == 0) {
-        cfg.gridDim = dim3(MAX_CLUSTER, 1, 1);
-        cfg.dynamicSmemBytes = draw_smem_bytes(a.V, 1);
-        int m = 0;
-        cudaError_t e = cudaOccupancyMaxPotentialClusterSize(&m, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        max_cluster = m < 1 ? 1 : m;
-    }
+    cfg.dynamicSmemBytes = draw_smem_bytes(a.V, 1);
+    int max_cluster = 0;  // largest cluster the device co-schedules for this kernel
+    const cudaError_t e = cache.max_cluster((const void*)kern, cfg, &max_cluster);
+    if (e != cudaSuccess) return e;
+    if (max_cluster < 1) max_cluster = 1;
     while (G > max_cluster) G >>= 1;
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
     cfg.dynamicSmemBytes = draw_smem_bytes(a.V, G);

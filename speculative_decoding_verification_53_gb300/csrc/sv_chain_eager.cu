@@ -322,41 +322,20 @@ size_t eager_smem_bytes(int V, int K, int G, int tsz, int dsz_logits, int probs,
 template <int TDT, int DDT, int DK>
 static cudaError_t launch_chain_eager_t(const ChainArgs& a, int G, cudaStream_t stream) {
     auto kern = chain_eager_kernel<TDT, DDT, DK>;
-    static int max_dyn = -1;
-    if (max_dyn < 0) {
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
-        if (e != cudaSuccess) return e;
-        const int m = optin - (int)fa.sharedSizeBytes;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, m);
-        if (e != cudaSuccess) return e;
-        max_dyn = m;
-    }
+    static KernelLaunchCache cache;
     if (a.K + 1 > EAGER_MAX_POS) return cudaErrorInvalidClusterSize;
     EagerArgs E;
     E.a = a;
     const size_t smem = eager_smem_bytes(a.V, a.K, G, TDT == DT_BF16 ? 2 : 4, DK == DK_LOGITS ? (DDT == DT_BF16 ? 2 : 4) : 0,
                                          DK == DK_PROBS ? 1 : 0, &E.t_bytes, &E.d_bytes, &E.probs_bytes);
-    if (smem > (size_t)max_dyn) return cudaErrorInvalidClusterSize;  // caller takes another kernel
-    static size_t cached_smem = 0;
-    static int cached_max = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    if (cached_smem != smem) {
-        cfg.gridDim = dim3(MAX_CLUSTER, 1, 1);
-        int m = 0;
-        cudaError_t e = cudaOccupancyMaxPotentialClusterSize(&m, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        cached_max = m;
-        cached_smem = smem;
-    }
-    if (cached_max < G) return cudaErrorInvalidClusterSize;
+    int maxc = 0;  // 0 when the shared memory does not fit: the caller takes another kernel
+    const cudaError_t e = cache.max_cluster((const void*)kern, cfg, &maxc);
+    if (e != cudaSuccess) return e;
+    if (maxc < G) return cudaErrorInvalidClusterSize;
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -279,41 +279,20 @@ size_t spec_smem_bytes(int V, int G, int tsz, int dsz, int* t_bytes, int* d_byte
 template <int TDT, int DDT, int DK>
 static cudaError_t launch_chain_spec_t(const ChainArgs& a, void* ws, int G, cudaStream_t stream) {
     auto kern = chain_spec_kernel<TDT, DDT, DK>;
-    static int max_dyn = -1;
-    if (max_dyn < 0) {
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
-        if (e != cudaSuccess) return e;
-        const int m = optin - (int)fa.sharedSizeBytes;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, m);
-        if (e != cudaSuccess) return e;
-        max_dyn = m;
-    }
+    static KernelLaunchCache cache;
     SpecArgs A;
     A.a = a;
     A.ws = reinterpret_cast<unsigned char*>(ws);
     A.wl = spec_ws_layout(a.B, a.K);
     const size_t smem = spec_smem_bytes(a.V, G, TDT == DT_BF16 ? 2 : 4, DDT == DT_BF16 ? 2 : 4, &A.t_bytes, &A.d_bytes);
-    if (smem > (size_t)max_dyn) return cudaErrorInvalidClusterSize;  // caller takes another kernel
-    static size_t cached_smem = 0;
-    static int cached_max = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    if (cached_smem != smem) {
-        cfg.gridDim = dim3(MAX_CLUSTER, 1, 1);
-        int m = 0;
-        cudaError_t e = cudaOccupancyMaxPotentialClusterSize(&m, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        cached_max = m;
-        cached_smem = smem;
-    }
-    if (cached_max < G) return cudaErrorInvalidClusterSize;
+    int maxc = 0;  // 0 when the shared memory does not fit: the caller takes another kernel
+    const cudaError_t e = cache.max_cluster((const void*)kern, cfg, &maxc);
+    if (e != cudaSuccess) return e;
+    if (maxc < G) return cudaErrorInvalidClusterSize;
     cfg.gridDim = dim3((unsigned)G, (unsigned)(a.K + 1), (unsigned)a.B);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

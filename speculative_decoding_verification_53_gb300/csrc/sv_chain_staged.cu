@@ -17,7 +17,7 @@
 namespace sv {
 
 template <int TDT, int DDT, int DK>
-__global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, const StageLayout L) {
+__global__ void __launch_bounds__(NT, 4) chain_staged_kernel(const ChainArgs a, const StageLayout L) {
     extern __shared__ __align__(128) unsigned char dsm[];
     // mbarriers: [0, nslot) target chunks, [nslot, 2 nslot) draft-logit chunks, [2 nslot] probabilities
     uint64_t* bars = reinterpret_cast<uint64_t*>(dsm);
@@ -42,11 +42,17 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     const unsigned char* dbase = reinterpret_cast<const unsigned char*>(a.draft) + (size_t)b * K * V * dsz;
     const int first = (K + 1 < L.nslot) ? K + 1 : L.nslot;  // positions staged up front
 
+    // Test hook (off unless stall_row is set): this row's first target copy is announced
+    // on its barrier but never issued, so the bounded wait for it runs out (after
+    // stall_ns) and the row reports a timeout; no copy is in flight for it.
+    const bool stall = b == a.stall_row;
+    const uint32_t wait_ns = stall ? a.stall_ns : WAIT_LIMIT_NS;
     auto issue_t = [&](int k) {
         const int s = k % L.nslot;
         fence_proxy_async();
         mbar_arrive_expect_tx(&tbar[s], (uint32_t)n * tsz);
-        if (n) bulk_g2s(slots + (size_t)s * L.slot_bytes, tbase + ((size_t)k * V + lo) * tsz, (uint32_t)n * tsz, &tbar[s]);
+        if (n && !(stall && k == 0))
+            bulk_g2s(slots + (size_t)s * L.slot_bytes, tbase + ((size_t)k * V + lo) * tsz, (uint32_t)n * tsz, &tbar[s]);
     };
     auto issue_d = [&](int k) {
         const int s = k % L.nslot;
@@ -80,9 +86,13 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
         for (int k = 0; k < first; ++k) issue_t(k);
     const bool greedy = !(T > 0.f);
     const float c = greedy ? 0.f : LOG2E / T;
-    const bool draft_rows = !greedy && DK == DK_LOGITS;  // draft-logit rows travel with the target rows
+    const bool draft_rows = !greedy && DK == DK_LOGITS;  // draft-logit rows take part in the statistics
+    // they travel with the target rows through the slots, or (d_direct: large batches, whose
+    // slots then hold twice as many rows on chip) are streamed from global memory
+    const bool d_direct = DK == DK_LOGITS && L.d_direct != 0;
+    const bool copy_d = draft_rows && !d_direct;
     if (threadIdx.x == 0) {
-        if (draft_rows)
+        if (copy_d)
             for (int k = 0; k < first && k < K; ++k) issue_d(k);
         if (DK == DK_PROBS && !greedy && L.prefetch_l2 && n)
             for (int k = 0; k < K; ++k) prefetch_l2(dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz);
@@ -90,7 +100,7 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     uint32_t tpar = 0, dpar = 0, tpend = 0, dpend = 0;  // per-slot phase parity / copy-in-flight bits
     for (int k = 0; k < first; ++k) {
         tpend |= 1u << k;
-        if (draft_rows && k < K) dpend |= 1u << k;
+        if (copy_d && k < K) dpend |= 1u << k;
     }
 
     int tok_bad = 0;
@@ -106,15 +116,15 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
         const int s = k % L.nslot;
         if (threadIdx.x == 0) {
             issue_t(k);
-            if (draft_rows && k < K) issue_d(k);
+            if (copy_d && k < K) issue_d(k);
         }
         tpend |= 1u << s;
-        if (draft_rows && k < K) dpend |= 1u << s;
+        if (copy_d && k < K) dpend |= 1u << s;
     };
     auto wait_slot = [&](int s) -> bool {  // both chunks of slot s (the draft one only if requested)
         bool ok = true;
         if (tpend & (1u << s)) {
-            ok = mbar_wait_bounded(&tbar[s], (tpar >> s) & 1u);
+            ok = mbar_wait_bounded_ns(&tbar[s], (tpar >> s) & 1u, wait_ns);
             tpar ^= 1u << s;
             tpend &= ~(1u << s);
         }
@@ -127,21 +137,27 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
     };
     int next_issue = first;
 
-    int phase = 0, j = -1, final_tok = -1, writer = 0;
+    // tmo: some wait of the row gave up (this CTA's, or a peer's flag seen in an exchange)
+    int phase = 0, j = -1, final_tok = -1, writer = 0, tmo = 0;
     for (int k = 0; k <= K && !invalid; ++k) {
         const int s = k % L.nslot;
         const int x = k < K ? s_tok[k] : -1;
         float qx_load = 0.f;  // q(x_k) for draft probabilities, loaded while the copy lands
         if (DK == DK_PROBS && !greedy && k < K && threadIdx.x == 0)
             qx_load = __ldg(reinterpret_cast<const float*>(dbase) + (size_t)k * V + x);
+        // a draft-logit row read directly is reduced while the target chunk lands
+        const unsigned char* drow = dbase + (size_t)k * V * dsz;
+        LSE ds_direct{neg_inf(), 0.f, 0};
+        if (d_direct && draft_rows && k < K) ds_direct = global_thread_lse<DDT>(drow, lo, hi, c);
         const int fail = __syncthreads_or(!wait_slot(s));
         if (DK == DK_PROBS && !greedy && k < K && threadIdx.x == 0) s_qx = qx_load;
         const unsigned char* tb = slots + (size_t)s * L.slot_bytes;
         const unsigned char* db = tb + L.t_bytes;
         if (greedy) {
             ArgMax am = smem_thread_argmax<TDT>(tb, n, lo);
-            if (fail) am.bad = 1;
+            if (fail) am.bad |= BAD_TIMEOUT;
             am = cluster_argmax(am, sc, phase);
+            if (am.bad & BAD_TIMEOUT) tmo = 1;
             if (am.bad || !(am.v > neg_inf()) || am.v == pos_inf()) { invalid = true; break; }
             if (k < K && x == am.i) {
                 if (threadIdx.x == 0) s_ap[k] = 1.f;
@@ -156,21 +172,23 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
         }
         LSE ts = smem_thread_lse<TDT>(tb, n, c);
         LSE ds{neg_inf(), 0.f, 0};
-        if (draft_rows && k < K) ds = smem_thread_lse<DDT>(db, n, c);
-        if (fail) ts.bad = 1;
+        if (draft_rows && k < K) ds = d_direct ? ds_direct : smem_thread_lse<DDT>(db, n, c);
+        if (fail) ts.bad |= BAD_TIMEOUT;
         float tx = 0.f, dx = 0.f;
         int has = 0;
         if (threadIdx.x == 0 && x >= lo && x < hi) {
             tx = smem_elem<TDT>(tb, x - lo);
-            if (draft_rows) dx = smem_elem<DDT>(db, x - lo);
+            if (draft_rows) dx = d_direct ? load_one<DDT>(drow, x) : smem_elem<DDT>(db, x - lo);
             has = 1;
         }
         const PosStats ps = cluster_pos_stats<DK == DK_LOGITS>(ts, ds, c, tx, dx, has, sc, phase);
+        if ((ps.t.bad | ps.d.bad) & BAD_TIMEOUT) tmo = 1;
         if (row_bad_s(ps.t) || (draft_rows && k < K && row_bad_s(ps.d))) { invalid = true; break; }
         const float inv_st = 1.f / ps.t.s;
         if (k == K) {  // every draft accepted: bonus token from p_K
             const StagedP<TDT> pw{tb, lo, c, ps.t.m, inv_st};
             const DrawResult d = cluster_draw(pw, lo, hi, s_u[K], tile_sum, sc, phase);
+            if (d.failed) { tmo = 1; invalid = true; break; }
             j = K;
             final_tok = d.token;
             writer = d.owner;
@@ -205,12 +223,19 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
             dfail = __syncthreads_or(!mbar_wait_bounded(pbar, 0u));
             qb = probs_area;
         }
-        const StagedResidual<TDT, DDT, DK> rw{tb, qb, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd};
-        DrawResult d = cluster_draw(rw, lo, hi, s_u[k], tile_sum, sc, phase, dfail);
-        if (d.failed) { invalid = true; break; }
+        DrawResult d;
+        if (d_direct) {
+            const StagedResidualD<TDT, DDT> rw{tb, drow, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd};
+            d = cluster_draw(rw, lo, hi, s_u[k], tile_sum, sc, phase, dfail);
+        } else {
+            const StagedResidual<TDT, DDT, DK> rw{tb, qb, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd};
+            d = cluster_draw(rw, lo, hi, s_u[k], tile_sum, sc, phase, dfail);
+        }
+        if (d.failed) { tmo = 1; invalid = true; break; }
         if (d.owner < 0) {  // the residual has no mass: draw from p_k
             const StagedP<TDT> pw{tb, lo, c, ps.t.m, inv_st};
             d = cluster_draw(pw, lo, hi, s_u[k], tile_sum, sc, phase);
+            if (d.failed) { tmo = 1; invalid = true; break; }
         }
         j = k;
         final_tok = d.token;
@@ -229,11 +254,15 @@ __global__ void __launch_bounds__(NT) chain_staged_kernel(const ChainArgs a, con
         if (a.out_accept_prob)
             for (int i = threadIdx.x; i < K; i += NT)
                 a.out_accept_prob[(size_t)b * K + i] = invalid ? -1.f : s_ap[i];
-        if (threadIdx.x == 0) a.out_count[b] = invalid ? 0 : j + 1;
+        if (threadIdx.x == 0) a.out_count[b] = invalid ? (tmo ? SV_COUNT_TIMEOUT : 0) : j + 1;
     }
-    // No trailing cluster barrier: peers only ever push into this CTA's inbox, and the
-    // last exchange of the (cluster-uniform) walk completed on this CTA's own barrier,
-    // so nothing is written into its shared memory once it gets here.
+    // Leave together: when every exchange completes, the walk is the same in every CTA of
+    // the cluster and nothing is pushed into a CTA after its last exchange; but a CTA
+    // whose bounded wait gave up may have left the walk early while a peer still pushes
+    // into its inbox.  Every wait before this barrier is bounded, so every CTA reaches
+    // it.  A CTA that saw a timeout then marks the row (after any other writer).
+    cluster_sync_all();
+    if (tmo && threadIdx.x == 0) a.out_count[b] = SV_COUNT_TIMEOUT;
 }
 
 size_t staged_smem_bytes(const StageLayout& L, int V, int G) {
@@ -243,37 +272,16 @@ size_t staged_smem_bytes(const StageLayout& L, int V, int G) {
 template <int TDT, int DDT, int DK>
 static cudaError_t launch_chain_staged_t(const ChainArgs& a, const StageLayout& L, int G, cudaStream_t stream) {
     auto kern = chain_staged_kernel<TDT, DDT, DK>;
-    static int max_dyn = -1;  // dynamic shared memory this kernel may request (opt-in limit minus static)
-    if (max_dyn < 0) {
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
-        if (e != cudaSuccess) return e;
-        const int m = optin - (int)fa.sharedSizeBytes;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, m);
-        if (e != cudaSuccess) return e;
-        max_dyn = m;
-    }
+    static KernelLaunchCache cache;
     const size_t smem = staged_smem_bytes(L, a.V, G);
-    if (smem > (size_t)max_dyn) return cudaErrorInvalidClusterSize;  // caller takes the streaming kernel
-    static size_t cached_smem = 0;
-    static int cached_max = 0;  // largest cluster the device co-schedules at that shared-memory size
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.stream = stream;
     cfg.dynamicSmemBytes = smem;
-    if (cached_smem != smem) {
-        cfg.gridDim = dim3(MAX_CLUSTER, 1, 1);
-        int m = 0;
-        cudaError_t e = cudaOccupancyMaxPotentialClusterSize(&m, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        cached_max = m;
-        cached_smem = smem;
-    }
-    if (cached_max < G) return cudaErrorInvalidClusterSize;  // caller picks another shape
+    int maxc = 0;  // largest co-scheduled cluster; 0 when the shared memory does not fit
+    const cudaError_t e = cache.max_cluster((const void*)kern, cfg, &maxc);
+    if (e != cudaSuccess) return e;
+    if (maxc < G) return cudaErrorInvalidClusterSize;  // caller picks another shape or kernel
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -146,10 +146,20 @@ __device__ __forceinline__ float vmax8(const float x[VEC]) {
 
 // ------------------------------------------------------ softmax statistics
 
+// Flags a partial result carries (bitwise or-ed through every reduction): BAD_DATA for
+// invalid data (NaN seen), BAD_TIMEOUT for a bounded wait (a bulk copy or a cluster
+// exchange) that gave up before completing.
+constexpr int BAD_DATA = 1;
+constexpr int BAD_TIMEOUT = 2;
+
+// NaN payloads of a pushed partial sum that stands for one of those flags.
+constexpr uint32_t NAN_BAD_DATA = 0x7fc00001u;
+constexpr uint32_t NAN_TIMEOUT = 0x7fc00002u;
+
 // Running (max m, sum s of 2^((l - m) * c)) of a set of logits, c = log2(e) / T.
 struct LSE {
     float m, s;
-    int bad;  // NaN seen
+    int bad;  // BAD_DATA / BAD_TIMEOUT flags
 };
 
 __device__ __forceinline__ void lse_merge(LSE& a, const LSE& b, float c) {
@@ -177,8 +187,8 @@ __device__ __forceinline__ void lse2_warp_reduce(LSE& a, LSE& b, float c) {
         sa += __shfl_xor_sync(0xffffffffu, sa, o);
         sb += __shfl_xor_sync(0xffffffffu, sb, o);
     }
-    a.bad = __any_sync(0xffffffffu, a.bad != 0) ? 1 : 0;
-    b.bad = __any_sync(0xffffffffu, b.bad != 0) ? 1 : 0;
+    a.bad = (int)__reduce_or_sync(0xffffffffu, (unsigned)a.bad);
+    b.bad = (int)__reduce_or_sync(0xffffffffu, (unsigned)b.bad);
     a.m = Ma;
     a.s = sa;
     b.m = Mb;
@@ -203,29 +213,30 @@ __device__ __forceinline__ void lse_warp_reduce(LSE& v, float c) {
     float s = (v.m > neg_inf()) ? v.s * ex2((v.m - M) * c) : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    v.bad = __any_sync(0xffffffffu, v.bad != 0) ? 1 : 0;
+    v.bad = (int)__reduce_or_sync(0xffffffffu, (unsigned)v.bad);
     v.m = M;
     v.s = s;
 }
 
-// One thread's pass over its vector steps of elements [lo, hi) of a row.
-template <int DT>
+// One thread's pass over its vector steps of elements [lo, hi) of a row (U vector steps
+// in flight).
+template <int DT, int U = UNROLL>
 __device__ __forceinline__ LSE thread_lse(const void* row, int lo, int hi, bool al, float c) {
     LSE acc{neg_inf(), 0.f, 0};
     const int v0 = lo / VEC, v1 = (hi + VEC - 1) / VEC;
-    for (int vb = v0 + (int)threadIdx.x; vb < v1; vb += NT * UNROLL) {
-        float x[UNROLL][VEC];
+    for (int vb = v0 + (int)threadIdx.x; vb < v1; vb += NT * U) {
+        float x[U][VEC];
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int v = vb + u * NT;
             if (v < v1) load8<DT>(row, v * VEC, hi, al, neg_inf(), x[u]);
         }
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int v = vb + u * NT;
             if (v >= v1) break;
             const float vm = vmax8(x[u]);
-            if (vm != vm) acc.bad = 1;
+            if (vm != vm) acc.bad = BAD_DATA;
             if (vm > acc.m) {
                 acc.s *= ex2((acc.m - vm) * c);
                 acc.m = vm;
@@ -246,7 +257,7 @@ __device__ __forceinline__ LSE thread_lse(const void* row, int lo, int hi, bool 
 struct ArgMax {
     float v;
     int i;
-    int bad;  // NaN seen
+    int bad;  // BAD_DATA / BAD_TIMEOUT flags
 };
 
 __device__ __forceinline__ void argmax_merge(ArgMax& a, const ArgMax& b) {
@@ -384,15 +395,23 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up and returns false
-// after a quarter of a second (global timer) or 2^22 tries, whichever comes first.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
+// after limit_ns nanoseconds (global timer) or 2^22 tries, whichever comes first.
+__device__ __forceinline__ bool mbar_wait_bounded_ns(uint64_t* bar, uint32_t parity, uint32_t limit_ns) {
+    const uint32_t hint = limit_ns < 1000000u ? limit_ns : 1000000u;
+    if (mbar_try_wait_for(bar, parity, hint)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 0; i < (1u << 22); ++i) {
-        if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
-        if (global_ns() - t0 > 250000000ull) break;
+        if (mbar_try_wait_for(bar, parity, hint)) return true;
+        if (global_ns() - t0 > (uint64_t)limit_ns) break;
     }
     return false;
+}
+
+// The default bound of every wait: a quarter of a second.
+constexpr uint32_t WAIT_LIMIT_NS = 250000000u;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_bounded_ns(bar, parity, WAIT_LIMIT_NS);
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -470,7 +489,8 @@ __device__ __forceinline__ void chunk_range(int V, int g, int G, int& lo, int& h
 // Sets up the inbox barriers; every thread of every CTA of the cluster calls it once,
 // before the first exchange.  Its cluster barrier makes every CTA's barriers exist
 // before any peer sends.  No global memory is touched (it may precede pdl_wait).
-__device__ __forceinline__ void xchg_init(BlockScratch& sc) {
+template <class SC>
+__device__ __forceinline__ void xchg_init(SC& sc) {
     if (threadIdx.x == 0) {
         mbar_init(&sc.xbar[0], 1);
         mbar_init(&sc.xbar[1], 1);
@@ -484,7 +504,8 @@ __device__ __forceinline__ void xchg_init(BlockScratch& sc) {
 // sets up this CTA's inbox barriers and arrives; xchg_ready waits for every CTA's
 // arrival and must come before the first exchange.  Every thread calls each once, in
 // that order, with no other cluster barrier between them.
-__device__ __forceinline__ void xchg_init_arrive(BlockScratch& sc) {
+template <class SC>
+__device__ __forceinline__ void xchg_init_arrive(SC& sc) {
     if (threadIdx.x == 0) {
         mbar_init(&sc.xbar[0], 1);
         mbar_init(&sc.xbar[1], 1);
@@ -499,17 +520,20 @@ __device__ __forceinline__ void xchg_ready() {
 
 // Exchange number `phase` uses inbox buffer phase & 1, whose barrier completes its
 // (phase >> 1)-th phase.  Thread 0 arms it with the bytes all G senders will deliver.
-__device__ __forceinline__ void xchg_arm(BlockScratch& sc, int phase, uint32_t bytes) {
+template <class SC>
+__device__ __forceinline__ void xchg_arm(SC& sc, int phase, uint32_t bytes) {
     if (threadIdx.x == 0) mbar_arrive_expect_tx(&sc.xbar[phase & 1], bytes);
 }
 
 // The receiver's barrier of this exchange, in CTA `peer`'s window.
-__device__ __forceinline__ uint32_t xchg_bar(BlockScratch& sc, int phase, uint32_t peer) {
+template <class SC>
+__device__ __forceinline__ uint32_t xchg_bar(SC& sc, int phase, uint32_t peer) {
     return dsmem_addr(&sc.xbar[phase & 1], peer);
 }
 
 // Bounded wait for this CTA's inbox of exchange `phase` to be complete.
-__device__ __forceinline__ bool xchg_wait(BlockScratch& sc, int phase) {
+template <class SC>
+__device__ __forceinline__ bool xchg_wait(SC& sc, int phase) {
     return mbar_wait_bounded(&sc.xbar[phase & 1], (uint32_t)(phase >> 1) & 1u);
 }
 
@@ -549,8 +573,8 @@ __device__ __forceinline__ void cluster_lse2(LSE& a, LSE& b, float c, BlockScrat
         LSE x{neg_inf(), 0.f, 0}, y{neg_inf(), 0.f, 0};
         if ((uint32_t)lane < G) {
             const float4 v = sc.inbox.part[buf][lane][0], f = sc.inbox.part[buf][lane][1];
-            x = LSE{v.x, v.y, __float_as_int(f.x) | (ok ? 0 : 1)};
-            y = LSE{v.z, v.w, __float_as_int(f.y) | (ok ? 0 : 1)};
+            x = LSE{v.x, v.y, __float_as_int(f.x) | (ok ? 0 : BAD_TIMEOUT)};
+            y = LSE{v.z, v.w, __float_as_int(f.y) | (ok ? 0 : BAD_TIMEOUT)};
         }
         lse_warp_reduce(x, c);
         lse_warp_reduce(y, c);
@@ -579,7 +603,7 @@ __device__ __forceinline__ ArgMax cluster_argmax(ArgMax a, BlockScratch& sc, int
                     make_float4(a.v, __int_as_float(a.i), __int_as_float(a.bad), 0.f), xchg_bar(sc, phase, lane));
     if (warp == 0) {
         const bool ok = __all_sync(0xffffffffu, xchg_wait(sc, phase));
-        ArgMax x{neg_inf(), 0x7fffffff, ok ? 0 : 1};
+        ArgMax x{neg_inf(), 0x7fffffff, ok ? 0 : BAD_TIMEOUT};
         for (int e = lane; e < G * NW; e += 32) {
             const float4 v = sc.inbox.part[buf][e / NW][e % NW];
             argmax_merge(x, ArgMax{v.x, __float_as_int(v.y), __float_as_int(v.z)});
@@ -666,9 +690,9 @@ struct DrawResult {
 // The draw given the tile sums of this CTA's chunk (tile t: elements lo + 256 t ..);
 // wf evaluates the weights of the one tile the owner CTA searches.  The caller has
 // synchronised the CTA after writing tile_sum.
-template <class WF>
+template <class WF, class SC>
 __device__ __forceinline__ DrawResult cluster_draw_from_tiles(const WF& wf, int lo, int hi, float u, const float* tile_sum,
-                                              BlockScratch& sc, int& phase, int fail_in = 0) {
+                                              SC& sc, int& phase, int fail_in = 0) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ntiles = (hi - lo + TILE - 1) / TILE;
     xchg_arm(sc, phase, cluster_size() * 8u);
@@ -813,13 +837,14 @@ struct InFlight : WF {
     static constexpr int kTilesInFlight = TB;
 };
 
-template <class WF>
-__device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float* tile_sum, BlockScratch& sc,
+template <class WF, class SC>
+__device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float* tile_sum, SC& sc,
                                    int& phase, int fail_in = 0) {
     constexpr int TB = TilesInFlight<WF>::value;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nw = (int)(blockDim.x >> 5);  // warps of this CTA
     const int ntiles = (hi - lo + TILE - 1) / TILE;
-    for (int t0 = warp * TB; t0 < ntiles; t0 += NW * TB) {
+    for (int t0 = warp * TB; t0 < ntiles; t0 += nw * TB) {
         float w[TB][VEC];
 #pragma unroll
         for (int i = 0; i < TB; ++i) {

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "spec_verify.h"
@@ -13,6 +14,10 @@ namespace sv {
 // Records a CUDA error for spec_verify_last_cuda_error (per calling thread), clears
 // the sticky launch error and returns SV_ERR_CUDA; cudaSuccess gives SV_OK.
 sv_status launch_status(cudaError_t e);
+
+// out_count value of a batch row whose kernel gave up a bounded wait (a bulk copy or
+// a cluster exchange that did not complete in time); 0 marks invalid data.
+constexpr int32_t SV_COUNT_TIMEOUT = -1;
 
 struct ChainArgs {
     const void* target;        // [B][K+1][V]
@@ -24,6 +29,11 @@ struct ChainArgs {
     int32_t* out_tokens;       // [B][K+1]
     int32_t* out_count;        // [B]
     float* out_accept_prob;    // [B][K] or nullptr
+    // Test hook of the staged walk (SPEC_VERIFY_TEST_STALL): batch row `stall_row` arms
+    // its first copy barrier without issuing the copy, so that its bounded wait runs out
+    // after `stall_ns`; -1 (the default) disables it.
+    int stall_row = -1;
+    uint32_t stall_ns = 0;
 };
 
 struct TreeArgs {
@@ -80,6 +90,7 @@ struct StageLayout {
     int t_bytes;      // offset of the draft chunk inside a slot
     int probs_bytes;  // separate area for the rejected position's draft-probability chunk
     int prefetch_l2;  // prefetch the draft-probability chunks into L2 at kernel start
+    int d_direct;     // draft-logit rows are read from global memory, not staged (slots hold the target only)
 };
 
 constexpr int STAGE_HEADER = 512;        // mbarriers (up to 2 * 16 + 1) at the start of dynamic shared memory
@@ -91,6 +102,18 @@ cudaError_t launch_chain_staged(const ChainArgs& a, const StageLayout& L, int td
 
 cudaError_t launch_tree_staged(const TreeArgs& a, const StageLayout& L, int tdt, int ddt, int dk, int cluster,
                                cudaStream_t stream);
+
+// Ring-streamed walk for large batches (sv_chain_ring.cu): every row resident, each
+// CTA's chunk streamed through `nstage` stages of 2048 elements (target piece, then the
+// draft piece at byte t_bytes).
+struct RingLayout {
+    int nstage;       // stages in the ring (1..8)
+    int stage_bytes;  // bytes per stage, 16-byte multiple
+    int t_bytes;      // offset of the draft piece inside a stage
+};
+size_t ring_smem_bytes(const RingLayout& L, int V, int G);
+cudaError_t launch_chain_ring(const ChainArgs& a, const RingLayout& L, int tdt, int ddt, int dk, int cluster,
+                              cudaStream_t stream);
 
 // All-positions-at-once chain kernel (small batches, K + 1 <= 16).
 cudaError_t launch_chain_eager(const ChainArgs& a, int tdt, int ddt, int dk, int cluster, cudaStream_t stream);
@@ -116,6 +139,42 @@ cudaError_t launch_tree(const TreeArgs& a, int tdt, int ddt, int dk, int cluster
 // Dynamic shared memory (tile sums of the draw) for a row split `cluster` ways.
 size_t draw_smem_bytes(int V, int cluster);
 
+
+// Launch facts of one kernel, kept per device ordinal and filled under a mutex, so
+// that several host threads and several devices may launch it: the kernel's function
+// attributes are set on each device on first use there (cluster sizes above 8, the
+// opt-in dynamic shared memory), and occupancy answers are cached per launch shape.
+class KernelLaunchCache {
+public:
+    // Sets the kernel up on the current device (once) and returns in *max_dyn the
+    // dynamic shared memory it may request there (opt-in limit minus its static part).
+    cudaError_t setup(const void* kern, int* max_dyn);
+    // Largest cluster the current device co-schedules for a launch with cfg's block
+    // size and dynamic shared memory (cudaOccupancyMaxPotentialClusterSize); 0 when
+    // that shared memory is beyond the kernel's limit.
+    cudaError_t max_cluster(const void* kern, const cudaLaunchConfig_t& cfg, int* out);
+    // Clusters of G CTAs resident at once for that launch shape (cudaOccupancyMaxActiveClusters).
+    cudaError_t active_clusters(const void* kern, const cudaLaunchConfig_t& cfg, int G, int* out);
+
+private:
+    static constexpr int kDevices = 64;
+    static constexpr int kEntries = 8;
+    struct Entry {
+        size_t smem;
+        unsigned threads;
+        int G;  // 0: max_cluster entry
+        int value;
+    };
+    struct Device {
+        bool ready = false;
+        int max_dyn = 0;
+        int used = 0;
+        Entry e[kEntries];
+    };
+    cudaError_t device(const void* kern, Device** out);
+    std::mutex mu_;
+    Device dev_[kDevices];
+};
 
 // Draft tokens x_k ~ softmax(draft_k / T) (argmax for greedy rows) for every (b, k).
 cudaError_t launch_draft_sample(const SampleArgs& a, int ddt, int num_sms, cudaStream_t stream);

@@ -147,37 +147,20 @@ __global__ void __launch_bounds__(NT) draft_sample_staged_kernel(const SampleArg
 template <int DDT>
 static cudaError_t sample_cluster(long long BK, int V, int& G_out) {
     auto kern = draft_sample_kernel<DDT>;
-    static int resident[5] = {-1, -1, -1, -1, -1};  // co-resident clusters for G = 1, 2, 4, 8, 16
-    static int cached_v = -1;
-    if (cached_v != V) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        for (int i = 0; i < 5; ++i) {
-            const int G = 1 << i;
-            cudaLaunchConfig_t cfg = {};
-            cfg.blockDim = dim3(NT, 1, 1);
-            cfg.gridDim = dim3((unsigned)G, 1, 1);
-            cfg.dynamicSmemBytes = draw_smem_bytes(V, G);
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = (unsigned)G;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-                (void)cudaGetLastError();
-                n = 0;
-            }
-            resident[i] = n;
-        }
-        cached_v = V;
-    }
+    static KernelLaunchCache cache;
     int G = 1;
     for (int i = 4; i >= 1; --i) {
         const int g = 1 << i;
-        if (V / g >= 2048 && resident[i] > 0 && BK <= resident[i]) {
+        if (V / g < 2048) continue;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(NT, 1, 1);
+        cfg.dynamicSmemBytes = draw_smem_bytes(V, g);
+        int resident = 0;  // clusters of g CTAs co-resident on the current device
+        if (cache.active_clusters((const void*)kern, cfg, g, &resident) != cudaSuccess) {
+            (void)cudaGetLastError();
+            resident = 0;
+        }
+        if (resident > 0 && BK <= resident) {
             G = g;
             break;
         }
@@ -215,19 +198,11 @@ template <int DDT>
 static cudaError_t launch_sample_staged_t(const SampleArgs& a, int num_sms, cudaStream_t stream) {
     auto kern = draft_sample_staged_kernel<DDT>;
     constexpr int dsz = DDT == DT_BF16 ? 2 : 4;
-    static int max_dyn = -1;
-    if (max_dyn < 0) {
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+    static KernelLaunchCache cache;
+    int max_dyn = 0;
+    {
+        const cudaError_t e = cache.setup((const void*)kern, &max_dyn);
         if (e != cudaSuccess) return e;
-        const int m = optin - (int)fa.sharedSizeBytes;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, m);
-        if (e != cudaSuccess) return e;
-        max_dyn = m;
     }
     auto chunk_bytes = [&](int G) {
         const size_t nvec = (size_t)(a.V + VEC - 1) / VEC, cmax = ((nvec + G - 1) / G) * VEC;
@@ -243,9 +218,8 @@ static cudaError_t launch_sample_staged_t(const SampleArgs& a, int num_sms, cuda
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.stream = stream;
     cfg.dynamicSmemBytes = smem;
-    cfg.gridDim = dim3(MAX_CLUSTER, 1, 1);
     int maxc = 0;  // largest cluster the device co-schedules at this shared-memory size
-    cudaError_t e = cudaOccupancyMaxPotentialClusterSize(&maxc, kern, &cfg);
+    cudaError_t e = cache.max_cluster((const void*)kern, cfg, &maxc);
     if (e != cudaSuccess) return e;
     if (maxc < G) {
         while (G > 1 && G > maxc) G >>= 1;

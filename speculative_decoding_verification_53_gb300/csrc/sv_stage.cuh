@@ -104,6 +104,58 @@ __device__ __forceinline__ LSE smem_thread_lse(const unsigned char* buf, int n, 
     return acc;
 }
 
+// (max, sum 2^((l - max) c)) of one thread's share of elements [lo, hi) of a row in global
+// memory (16-byte aligned; lo a multiple of 8), online: four 16-byte vectors in flight per
+// thread, kept packed until used (bf16 rows: the maximum of a vector by max.bf16x2, no
+// unpacking), the running sum rescaled only when the maximum grows.
+template <int DT>
+__device__ __forceinline__ LSE global_thread_lse(const void* row, int lo, int hi, float c) {
+    if (DT != DT_BF16) return thread_lse<DT, 2>(row, lo, hi, true, c);
+    constexpr int U = 4;
+    LSE acc{neg_inf(), 0.f, 0};
+    float mc = 0.f, s0 = 0.f, s1 = 0.f;
+    const unsigned short* r = reinterpret_cast<const unsigned short*>(row);
+    for (int e0 = lo + (int)threadIdx.x * VEC; e0 < hi; e0 += NT * VEC * U) {
+        uint4 v[U];
+        bool full[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * NT * VEC;
+            full[u] = e + VEC <= hi;
+            v[u] = full[u] ? ld_nc_v4(r + e) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+            if (!full[u] && e < hi) {  // a ragged last vector: the elements before hi, -inf after
+                uint32_t w[4] = {0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u};
+                for (int j = 0; j < VEC && e + j < hi; ++j) {
+                    const uint32_t h = (uint32_t)__ldg(r + e + j);
+                    w[j >> 1] = (j & 1) ? ((w[j >> 1] & 0x0000ffffu) | (h << 16)) : ((w[j >> 1] & 0xffff0000u) | h);
+                }
+                v[u] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t pm = bmax2_nan(bmax2_nan(v[u].x, v[u].y), bmax2_nan(v[u].z, v[u].w));
+            const float vm = fmax_nan(bf16_lo(pm), bf16_hi(pm));
+            if (vm != vm) acc.bad = BAD_DATA;
+            if (vm > acc.m) {
+                const float f = ex2((acc.m - vm) * c);
+                s0 *= f;
+                s1 *= f;
+                acc.m = vm;
+                mc = vm * c;
+            }
+            if (acc.m > neg_inf()) {
+                s0 += ex2(fmaf(bf16_lo(v[u].x), c, -mc)) + ex2(fmaf(bf16_lo(v[u].y), c, -mc)) +
+                      ex2(fmaf(bf16_lo(v[u].z), c, -mc)) + ex2(fmaf(bf16_lo(v[u].w), c, -mc));
+                s1 += ex2(fmaf(bf16_hi(v[u].x), c, -mc)) + ex2(fmaf(bf16_hi(v[u].y), c, -mc)) +
+                      ex2(fmaf(bf16_hi(v[u].z), c, -mc)) + ex2(fmaf(bf16_hi(v[u].w), c, -mc));
+            }
+        }
+    }
+    acc.s = s0 + s1;
+    return acc;
+}
+
 // argmax (lowest index on ties) of the n staged elements; indices reported as lo + local.
 template <int DT>
 __device__ __forceinline__ ArgMax smem_thread_argmax(const unsigned char* buf, int n, int lo) {
@@ -123,6 +175,20 @@ __device__ __forceinline__ ArgMax smem_thread_argmax(const unsigned char* buf, i
         }
     }
     return acc;
+}
+
+// The sum slot of a pushed (max, sum) partial: the sum, or a NaN whose payload names
+// the flag (a timeout takes precedence over invalid data).
+__device__ __forceinline__ float flagged_sum(const LSE& s) {
+    if (s.bad & BAD_TIMEOUT) return __uint_as_float(NAN_TIMEOUT);
+    if (s.bad) return __uint_as_float(NAN_BAD_DATA);
+    return s.s;
+}
+
+// Flags of a received sum slot (0 for a number).
+__device__ __forceinline__ int sum_flags(float v) {
+    if (v == v) return 0;
+    return __float_as_uint(v) == NAN_TIMEOUT ? BAD_TIMEOUT : BAD_DATA;
 }
 
 __device__ __forceinline__ bool row_bad_s(const LSE& s) {
@@ -156,8 +222,7 @@ __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, flo
         lse_warp_reduce(t, c);
     }
     if (lane < G) {
-        const float4 v = make_float4(t.m, t.bad ? __int_as_float(0x7fffffff) : t.s, TWO ? d.m : neg_inf(),
-                                     (TWO && d.bad) ? __int_as_float(0x7fffffff) : (TWO ? d.s : 0.f));
+        const float4 v = make_float4(t.m, flagged_sum(t), TWO ? d.m : neg_inf(), TWO ? flagged_sum(d) : 0.f);
         st_async_v4(dsmem_addr(&sc.inbox.part[buf][me][warp], (uint32_t)lane), v, xchg_bar(sc, phase, lane));
     }
     if (warp == 0) {
@@ -182,8 +247,8 @@ __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, flo
         for (int i = 0; i < 4; ++i) {
             Mt = fmaxf(Mt, v[i].x);
             Md = fmaxf(Md, v[i].z);
-            bt |= v[i].y != v[i].y;
-            bd |= v[i].w != v[i].w;
+            bt |= sum_flags(v[i].y);
+            bd |= sum_flags(v[i].w);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -201,8 +266,9 @@ __device__ __forceinline__ PosStats cluster_pos_stats(LSE t, LSE d, float c, flo
             St += __shfl_xor_sync(0xffffffffu, St, o);
             if (TWO) Sd += __shfl_xor_sync(0xffffffffu, Sd, o);
         }
-        bt = (__any_sync(0xffffffffu, bt) || !ok) ? 1 : 0;  // a wait that gave up voids the row
-        bd = __any_sync(0xffffffffu, bd) ? 1 : 0;
+        // a wait that gave up voids the row (and is reported as a timeout)
+        bt = (int)__reduce_or_sync(0xffffffffu, (unsigned)bt) | (ok ? 0 : BAD_TIMEOUT);
+        bd = (int)__reduce_or_sync(0xffffffffu, (unsigned)bd) | (ok ? 0 : BAD_TIMEOUT);
         float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
         if (lane < G) gv = sc.inbox.gath[buf][lane];
         const unsigned owners = __ballot_sync(0xffffffffu, gv.z != 0.f);
@@ -237,6 +303,29 @@ struct StagedP {  // w = p = 2^((l - m) c) / S
         const float mc = m * c;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) w[j] = ex2(fmaf(l[j], c, -mc)) * inv_s;
+    }
+};
+
+// w = max(0, p - q) with the target chunk staged and the draft-logit row read from
+// global memory (it was streamed for its statistics just before, so from L2).
+template <int TDT, int DDT>
+struct StagedResidualD {
+    static constexpr int kTilesInFlight = 2;  // global loads: two tiles in flight per warp
+    const unsigned char* tb;
+    const void* drow;
+    int lo;
+    float c, mt, inv_st, md, inv_sd;
+    __device__ __forceinline__ void eval8(int e0, int hi, float w[VEC]) const {
+        float l[VEC], d[VEC];
+        smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
+        load8<DDT>(drow, e0, hi, true, neg_inf(), d);
+        const float mtc = mt * c, mdc = md * c;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            const float p = ex2(fmaf(l[j], c, -mtc)) * inv_st;
+            const float q = ex2(fmaf(d[j], c, -mdc)) * inv_sd;
+            w[j] = fmaxf(p - q, 0.f);
+        }
     }
 };
 

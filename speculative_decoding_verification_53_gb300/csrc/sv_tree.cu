@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(NT) tree_kernel(const TreeArgs a) {
     if (!invalid) invalid = s_flag != 0;
     __syncthreads();
 
-    int phase = 0, emitted = 0, cur = -1, writer = 0;
+    // tmo: some wait of the row gave up (this CTA's, or a peer's flag seen in an exchange)
+    int phase = 0, emitted = 0, cur = -1, writer = 0, tmo = 0;
     while (!invalid) {
         const int row = cur + 1;
         const void* trow = (const char*)a.target + ((size_t)b * (N + 1) + row) * (size_t)V * tsz;
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(NT) tree_kernel(const TreeArgs a) {
         if (greedy) {
             ArgMax am = thread_argmax<TDT>(trow, lo, hi, at);
             am = cluster_argmax(am, sc, phase);
+            if (am.bad & BAD_TIMEOUT) tmo = 1;
             if (am.bad || !(am.v > neg_inf()) || am.v == pos_inf()) { invalid = true; break; }
             int next = -1;
             for (int q = 0; q < nchild; ++q)
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(NT) tree_kernel(const TreeArgs a) {
         LSE ds{neg_inf(), 0.f, 0};
         if (DK == DK_LOGITS && nchild > 0) ds = thread_lse<DDT>(drow, lo, hi, ad, c);
         cluster_lse2(ts, ds, c, sc, phase);
+        if ((ts.bad | ds.bad) & BAD_TIMEOUT) tmo = 1;
         if (tree_row_bad(ts) || (DK == DK_LOGITS && nchild > 0 && tree_row_bad(ds))) { invalid = true; break; }
         const TreeRow<TDT, DDT, DK> rw{trow, drow, c, ts.m, 1.f / ts.s, ds.m, DK == DK_LOGITS ? 1.f / ds.s : 0.f,
                                        at, ad};
@@ -218,6 +221,11 @@ __global__ void __launch_bounds__(NT) tree_kernel(const TreeArgs a) {
                 }
             }
             const float2 tot = cluster_sum2(part, sc, phase);
+            if (tot.x != tot.x) {  // the exchange gave up (NaN sums)
+                tmo = 1;
+                invalid = true;
+                break;
+            }
             if (threadIdx.x == 0) {
                 // without replacement the tried token leaves q and q is renormalised;
                 // i.i.d. siblings leave q as it is (no token recorded, no rescale)
@@ -245,6 +253,11 @@ __global__ void __launch_bounds__(NT) tree_kernel(const TreeArgs a) {
         slot_uniforms(a.seed, a.offset, (uint64_t)b, (uint64_t)row, r_unused, u);
         const TreeDrawWeights<TDT, DDT, DK> dw{rw, &hs, hs.n > 0};
         const DrawResult d = cluster_draw(dw, lo, hi, u, tile_sum, sc, phase);
+        if (d.failed || d.owner < 0) {
+            tmo = d.failed ? 1 : tmo;
+            invalid = true;
+            break;
+        }
         if (threadIdx.x == 0) s_out[emitted] = d.token;
         ++emitted;
         writer = d.owner;
@@ -257,34 +270,29 @@ __global__ void __launch_bounds__(NT) tree_kernel(const TreeArgs a) {
         int32_t* op = a.out_path + (size_t)b * D;
         for (int i = threadIdx.x; i <= D; i += NT) ot[i] = (!invalid && i < emitted) ? s_out[i] : -1;
         for (int i = threadIdx.x; i < D; i += NT) op[i] = (!invalid && i < emitted - 1) ? s_path[i] : -1;
-        if (threadIdx.x == 0) a.out_count[b] = invalid ? 0 : emitted;
+        if (threadIdx.x == 0) a.out_count[b] = invalid ? (tmo ? SV_COUNT_TIMEOUT : 0) : emitted;
     }
-    // No trailing cluster barrier: peers only ever push into this CTA's inbox, and the
-    // last exchange (the same sequence in every CTA of the cluster) completed on this
-    // CTA's own barrier, so nothing is written into its shared memory any more.
+    // Leave together: when every exchange completes, the walk is the same in every CTA of
+    // the cluster and nothing is pushed into a CTA after its last exchange; but a CTA
+    // whose bounded wait gave up may have left the walk early while a peer still pushes
+    // into its inbox.  Every wait before this barrier is bounded, so every CTA reaches
+    // it.  A CTA that saw a timeout then marks the row (after any other writer).
+    cluster_sync_all();
+    if (tmo && threadIdx.x == 0) a.out_count[b] = SV_COUNT_TIMEOUT;
 }
 
 template <int TDT, int DDT, int DK>
 static cudaError_t launch_tree_t(const TreeArgs& a, int G, cudaStream_t stream) {
     auto kern = tree_kernel<TDT, DDT, DK>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    static int max_cluster = 0;  // largest cluster the device co-schedules for this kernel
+    static KernelLaunchCache cache;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.stream = stream;
-    if (max_cluster == 0) {
-        cfg.gridDim = dim3(MAX_CLUSTER, 1, 1);
-        cfg.dynamicSmemBytes = draw_smem_bytes(a.V, 1);
-        int m = 0;
-        cudaError_t e = cudaOccupancyMaxPotentialClusterSize(&m, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        max_cluster = m < 1 ? 1 : m;
-    }
+    cfg.dynamicSmemBytes = draw_smem_bytes(a.V, 1);
+    int max_cluster = 0;  // largest cluster the device co-schedules for this kernel
+    const cudaError_t e = cache.max_cluster((const void*)kern, cfg, &max_cluster);
+    if (e != cudaSuccess) return e;
+    if (max_cluster < 1) max_cluster = 1;
     while (G > max_cluster) G >>= 1;
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
     cfg.dynamicSmemBytes = draw_smem_bytes(a.V, G);

@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
     const bool with_draft = !greedy;
     complete_issue(0, 0, with_draft);
     bool invalid = __syncthreads_or(bad) != 0;
+    int tmo = 0;  // some wait of the row gave up (this CTA's, or a peer's flag seen in an exchange)
     if (!invalid) {
         // every node's depth must fit max_depth: depths by pointer jumping on (count, target)
         // pairs, read / barrier / write rounds; a node stops at the root or beyond D
@@ -274,8 +275,9 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
         int next = -1;
         if (greedy) {
             ArgMax am = smem_thread_argmax<TDT>(tb, n, lo);
-            if (fail) am.bad = 1;
+            if (fail) am.bad |= BAD_TIMEOUT;
             am = cluster_argmax(am, sc, phase);
+            if (am.bad & BAD_TIMEOUT) tmo = 1;
             if (am.bad || !(am.v > neg_inf()) || am.v == pos_inf()) { invalid = true; break; }
             for (int q = 0; q < nchild; ++q)
                 if (s_tok[s_child[q]] == am.i) { next = s_child[q]; break; }
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
             LSE ts = smem_thread_lse<TDT>(tb, n, c);
             LSE ds{neg_inf(), 0.f, 0};
             if (DK == DK_LOGITS && nchild > 0) ds = smem_thread_lse<DDT>(db, n, c);
-            if (fail) ts.bad = 1;
+            if (fail) ts.bad |= BAD_TIMEOUT;
             if (gat) {
                 s_rt[threadIdx.x] = g_rt;
                 s_rd[threadIdx.x] = g_rd;
@@ -298,6 +300,7 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
             }
             // (the combine's barriers publish the gathered values, the mask and the history)
             const PosStats ps = cluster_pos_stats<DK == DK_LOGITS>(ts, ds, c, 0.f, 0.f, 0, sc, phase);
+            if ((ps.t.bad | ps.d.bad) & BAD_TIMEOUT) tmo = 1;
             if (row_bad_s(ps.t) || (DK == DK_LOGITS && nchild > 0 && row_bad_s(ps.d))) { invalid = true; break; }
             const float inv_st = 1.f / ps.t.s;
             const float inv_sd = (DK == DK_LOGITS && nchild > 0) ? 1.f / ps.d.s : 0.f;
@@ -353,6 +356,11 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
                     }
                 }
                 const float2 tot = cluster_sum2(part, sc, phase);
+                if (tot.x != tot.x) {  // the exchange gave up (NaN sums)
+                    tmo = 1;
+                    invalid = true;
+                    break;
+                }
                 if (threadIdx.x == 0) {
                     // without replacement the tried token leaves q and q is renormalised;
                     // i.i.d. siblings leave q as it is (no token recorded, no rescale)
@@ -386,6 +394,11 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
             if (next < 0) {  // no child kept (or a leaf): the last token from the current p
                 const StagedNodeP<TDT> pw{tb, wbuf, lo, c, node.mtc, inv_st, wmat};
                 const DrawResult d = cluster_draw(pw, lo, hi, s_u[row], tile_sum, sc, phase);
+                if (d.failed || d.owner < 0) {
+                    tmo = d.failed ? 1 : tmo;
+                    invalid = true;
+                    break;
+                }
                 if (threadIdx.x == 0) s_out[emitted] = d.token;
                 ++emitted;
                 writer = d.owner;
@@ -423,30 +436,26 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
         int32_t* op = a.out_path + (size_t)b * D;
         for (int i = threadIdx.x; i <= D; i += NT) ot[i] = (!invalid && i < emitted) ? s_out[i] : -1;
         for (int i = threadIdx.x; i < D; i += NT) op[i] = (!invalid && i < emitted - 1) ? s_path[i] : -1;
-        if (threadIdx.x == 0) a.out_count[b] = invalid ? 0 : emitted;
+        if (threadIdx.x == 0) a.out_count[b] = invalid ? (tmo ? SV_COUNT_TIMEOUT : 0) : emitted;
     }
-    // No trailing cluster barrier: peers only ever push into this CTA's inbox, and the
-    // last exchange (the same sequence in every CTA of the cluster) completed on this
-    // CTA's own barrier, so nothing is written into its shared memory any more.
+    // Leave together: when every exchange completes, the walk is the same in every CTA of
+    // the cluster and nothing is pushed into a CTA after its last exchange; but a CTA
+    // whose bounded wait gave up may have left the walk early while a peer still pushes
+    // into its inbox.  Every wait before this barrier is bounded, so every CTA reaches
+    // it.  A CTA that saw a timeout then marks the row (after any other writer).
+    cluster_sync_all();
+    if (tmo && threadIdx.x == 0) a.out_count[b] = SV_COUNT_TIMEOUT;
 }
 
 
 template <int TDT, int DDT, int DK>
 static cudaError_t launch_tree_staged_t(const TreeArgs& a, const StageLayout& L, int G, cudaStream_t stream) {
     auto kern = tree_staged_kernel<TDT, DDT, DK>;
-    static int max_dyn = -1;
-    if (max_dyn < 0) {
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+    static KernelLaunchCache cache;
+    int max_dyn = 0;
+    {
+        const cudaError_t e = cache.setup((const void*)kern, &max_dyn);
         if (e != cudaSuccess) return e;
-        const int m = optin - (int)fa.sharedSizeBytes;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, m);
-        if (e != cudaSuccess) return e;
-        max_dyn = m;
     }
     StageLayout Lk = L;
     size_t smem = STAGE_HEADER + tree_array_bytes(a.N) + (size_t)Lk.nslot * Lk.slot_bytes + tree_work_bytes(a.V, G) +
@@ -456,21 +465,14 @@ static cudaError_t launch_tree_staged_t(const TreeArgs& a, const StageLayout& L,
         smem -= Lk.slot_bytes;
     }
     if (smem > (size_t)max_dyn) return cudaErrorInvalidClusterSize;  // caller takes the streaming kernel
-    static size_t cached_smem = 0;
-    static int cached_max = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    if (cached_smem != smem) {
-        cfg.gridDim = dim3(MAX_CLUSTER, 1, 1);
-        int m = 0;
-        cudaError_t e = cudaOccupancyMaxPotentialClusterSize(&m, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        cached_max = m;
-        cached_smem = smem;
-    }
-    if (cached_max < G) return cudaErrorInvalidClusterSize;
+    int maxc = 0;
+    const cudaError_t e = cache.max_cluster((const void*)kern, cfg, &maxc);
+    if (e != cudaSuccess) return e;
+    if (maxc < G) return cudaErrorInvalidClusterSize;
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

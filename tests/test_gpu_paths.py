@@ -1,7 +1,7 @@
 """Each kernel family (all-positions staged, position-parallel, shared-memory staged walk,
-register streaming)
-against the oracle on the same aligned inputs; the family is forced through the
-SPEC_VERIFY_PATH environment variable in a child process."""
+register streaming, ring-streamed walk) against the oracle on the same aligned inputs;
+the family is forced through the SPEC_VERIFY_PATH environment variable in a child
+process."""
 import os
 import subprocess
 import sys
@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-@pytest.mark.parametrize("path", ["eager", "spec", "staged", "stream"])
+@pytest.mark.parametrize("path", ["eager", "spec", "staged", "stream", "ring"])
 def test_kernel_family_matches_oracle(path):
     env = dict(os.environ, SPEC_VERIFY_PATH=path)
     res = subprocess.run([sys.executable, os.path.join(HERE, "_path_check.py")], env=env, capture_output=True,

@@ -49,7 +49,7 @@ def _noalloc_call(lib, w, t, d, tok, temp, seed, offset):
     return ot.cpu().numpy(), oc.cpu().numpy(), ap.cpu().numpy()
 
 
-@pytest.mark.parametrize("case", ["single_stream", "mixed", "tiny_fp32"])
+@pytest.mark.parametrize("case", ["single_stream", "mixed", "tiny_fp32", "moderate"])
 def test_noalloc_matches_workspace_entry_point(case):
     import torch
     import speculative_decoding_verification_53_gb300 as sv
@@ -60,6 +60,8 @@ def test_noalloc_matches_workspace_entry_point(case):
         w = synth.single_stream(seed=31, B=2)
     elif case == "mixed":
         w = synth.mixed_batch(seed=32, B=3, K=5, V=32000)
+    elif case == "moderate":  # a batch the automatic kernel choice walks (no scratch used)
+        w = synth.mixed_batch(seed=34, B=128, K=5, V=32000)
     else:
         w = synth.tiny_chain(seed=33, V=1024, K=4, B=1)
     t, d, tok, temp = _dev(w["target"]), _dev(w["draft"]), _dev(w["tokens"]), _dev(w["temperature"])
@@ -86,4 +88,32 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     B, K, V = 65535, 64, 152064
     assert sv.spec_verify_workspace_size(B, K, V) > (256 << 10)
     st = lib.spec_verify_chain_noalloc(vp, 1, vp, 1, 1, vp, vp, B, K, V, 0, 0, vp, vp, None, None)
+    assert st == sv.SV_ERR_UNSUPPORTED
+
+
+def test_noalloc_scratch_limit_edges():
+    """B = 32768 rows need exactly the 256 KiB of scratch and run (matching the
+    workspace entry point); one row more is refused before anything is launched."""
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    lib = sv.lib()
+    B, K, V = 32768, 1, 16
+    assert sv.spec_verify_workspace_size(B, K, V) == (256 << 10)
+    assert sv.spec_verify_workspace_size(B + 1, K, V) > (256 << 10)
+    w = synth.tiny_chain(seed=35, V=V, K=K, B=B)
+    t, d, tok, temp = _dev(w["target"]), _dev(w["draft"]), _dev(w["tokens"]), _dev(w["temperature"])
+    ws = torch.zeros(sv.spec_verify_workspace_size(B, K, V), dtype=torch.uint8, device="cuda")
+    for offset in (0, 1):
+        rt, rc, _ = sv.spec_verify_chain(t, d, tok, temp, 3, offset, draft_kind="logits", workspace=ws)
+        torch.cuda.synchronize()
+        nt, nc, _ = _noalloc_call(lib, w, t, d, tok, temp, 3, offset)
+        rt, rc = rt.cpu().numpy(), rc.cpu().numpy()
+        same = (nt == rt).all(1) & (nc == rc)
+        if not same.all():
+            rows = np.nonzero(~same)[0]
+            o = oracle_chain(w, seed=3, offset=offset, rows=rows)
+            assert (o["margin"] < MARGIN).all(), rows[:8]
+        assert (nc >= 1).all()
+    vp = ctypes.c_void_p(16)  # never dereferenced: the size check comes first
+    st = lib.spec_verify_chain_noalloc(vp, 0, vp, 0, 1, vp, vp, B + 1, K, V, 0, 0, vp, vp, None, None)
     assert st == sv.SV_ERR_UNSUPPORTED
