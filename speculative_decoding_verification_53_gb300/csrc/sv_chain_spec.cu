@@ -88,7 +88,7 @@ __device__ __forceinline__ void spec_finish(const SpecArgs& A, int b, bool tok_b
 
 
 template <int TDT, int DDT, int DK>
-__global__ void __launch_bounds__(NT) chain_spec_kernel(const SpecArgs A) {
+__global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
     const ChainArgs& a = A.a;
     extern __shared__ __align__(128) unsigned char dsm[];
     uint64_t* tbar = reinterpret_cast<uint64_t*>(dsm);

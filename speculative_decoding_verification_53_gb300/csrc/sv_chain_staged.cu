@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(NT, 4) chain_staged_kernel(const ChainArgs a, 
     if (threadIdx.x == 0) {
         if (copy_d)
             for (int k = 0; k < first && k < K; ++k) issue_d(k);
+        if (d_direct && draft_rows && K > 0 && n) prefetch_l2(dbase + (size_t)lo * dsz, (uint32_t)n * dsz);
         if (DK == DK_PROBS && !greedy && L.prefetch_l2 && n)
             for (int k = 0; k < K; ++k) prefetch_l2(dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz);
     }
@@ -117,6 +118,9 @@ __global__ void __launch_bounds__(NT, 4) chain_staged_kernel(const ChainArgs a, 
         if (threadIdx.x == 0) {
             issue_t(k);
             if (copy_d && k < K) issue_d(k);
+            // a draft-logit row streamed directly is announced to L2 now: its statistics then
+            // stream from L2 while the target chunk lands (no extra bytes: the row is read anyway)
+            if (d_direct && draft_rows && k < K && n) prefetch_l2(dbase + ((size_t)k * V + lo) * dsz, (uint32_t)n * dsz);
         }
         tpend |= 1u << s;
         if (copy_d && k < K) dpend |= 1u << s;

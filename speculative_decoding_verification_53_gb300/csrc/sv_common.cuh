@@ -36,6 +36,57 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Two fp32 lanes per instruction (Blackwell's packed f32x2 arithmetic).  Each lane is
+// rounded exactly as the scalar instruction would round it; the exponential loops use
+// these to halve their FMA and add instructions (they are issue-bound, not exp-bound).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Sum of 2^(x_j c - mc) over eight values, as two packed accumulators.
+__device__ __forceinline__ void exp2_sum8(const float x[8], float c, float mc, float2& a0, float2& a1) {
+    const float2 cc = make_float2(c, c), mm = make_float2(-mc, -mc);
+    const float2 y0 = ffma2(make_float2(x[0], x[1]), cc, mm), y1 = ffma2(make_float2(x[2], x[3]), cc, mm);
+    const float2 y2 = ffma2(make_float2(x[4], x[5]), cc, mm), y3 = ffma2(make_float2(x[6], x[7]), cc, mm);
+    a0 = fadd2(a0, fadd2(make_float2(ex2(y0.x), ex2(y0.y)), make_float2(ex2(y1.x), ex2(y1.y))));
+    a1 = fadd2(a1, fadd2(make_float2(ex2(y2.x), ex2(y2.y)), make_float2(ex2(y3.x), ex2(y3.y))));
+}
+
+// Eight probabilities 2^(x_j c - mc) * inv_s.
+__device__ __forceinline__ void exp2_scale8(const float x[8], float c, float mc, float inv_s, float w[8]) {
+    const float2 cc = make_float2(c, c), mm = make_float2(-mc, -mc), ss = make_float2(inv_s, inv_s);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        const float2 y = ffma2(make_float2(x[j], x[j + 1]), cc, mm);
+        const float2 p = fmul2(make_float2(ex2(y.x), ex2(y.y)), ss);
+        w[j] = p.x;
+        w[j + 1] = p.y;
+    }
+}
+
 // Maximum that propagates NaN (a NaN anywhere in a row must mark the row invalid).
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float d;
@@ -242,10 +293,9 @@ __device__ __forceinline__ LSE thread_lse(const void* row, int lo, int hi, bool 
                 acc.m = vm;
             }
             if (acc.m > neg_inf()) {
-                float s = 0.f;
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) s += ex2((x[u][j] - acc.m) * c);
-                acc.s += s;
+                float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+                exp2_sum8(x[u], c, acc.m * c, a0, a1);
+                acc.s += (a0.x + a0.y) + (a1.x + a1.y);
             }
         }
     }

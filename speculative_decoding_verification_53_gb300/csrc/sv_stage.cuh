@@ -91,16 +91,13 @@ __device__ __forceinline__ LSE smem_thread_lse(const unsigned char* buf, int n, 
     LSE acc{m, 0.f, m != m ? 1 : 0};
     if (!(m > neg_inf()) || acc.bad) return acc;
     const float mc = m * c;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0;
     for (int e = (int)threadIdx.x * VEC; e < n; e += NT * VEC) {
         float x[VEC];
         smem_load8<DT>(buf, e, n, neg_inf(), x);
-        s0 += ex2(fmaf(x[0], c, -mc)) + ex2(fmaf(x[4], c, -mc));
-        s1 += ex2(fmaf(x[1], c, -mc)) + ex2(fmaf(x[5], c, -mc));
-        s2 += ex2(fmaf(x[2], c, -mc)) + ex2(fmaf(x[6], c, -mc));
-        s3 += ex2(fmaf(x[3], c, -mc)) + ex2(fmaf(x[7], c, -mc));
+        exp2_sum8(x, c, mc, a0, a1);
     }
-    acc.s = (s0 + s1) + (s2 + s3);
+    acc.s = (a0.x + a0.y) + (a1.x + a1.y);
     return acc;
 }
 
@@ -113,7 +110,8 @@ __device__ __forceinline__ LSE global_thread_lse(const void* row, int lo, int hi
     if (DT != DT_BF16) return thread_lse<DT, 2>(row, lo, hi, true, c);
     constexpr int U = 4;
     LSE acc{neg_inf(), 0.f, 0};
-    float mc = 0.f, s0 = 0.f, s1 = 0.f;
+    float mc = 0.f;
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0;
     const unsigned short* r = reinterpret_cast<const unsigned short*>(row);
     for (int e0 = lo + (int)threadIdx.x * VEC; e0 < hi; e0 += NT * VEC * U) {
         uint4 v[U];
@@ -139,20 +137,19 @@ __device__ __forceinline__ LSE global_thread_lse(const void* row, int lo, int hi
             if (vm != vm) acc.bad = BAD_DATA;
             if (vm > acc.m) {
                 const float f = ex2((acc.m - vm) * c);
-                s0 *= f;
-                s1 *= f;
+                a0 = fmul2(a0, make_float2(f, f));
+                a1 = fmul2(a1, make_float2(f, f));
                 acc.m = vm;
                 mc = vm * c;
             }
             if (acc.m > neg_inf()) {
-                s0 += ex2(fmaf(bf16_lo(v[u].x), c, -mc)) + ex2(fmaf(bf16_lo(v[u].y), c, -mc)) +
-                      ex2(fmaf(bf16_lo(v[u].z), c, -mc)) + ex2(fmaf(bf16_lo(v[u].w), c, -mc));
-                s1 += ex2(fmaf(bf16_hi(v[u].x), c, -mc)) + ex2(fmaf(bf16_hi(v[u].y), c, -mc)) +
-                      ex2(fmaf(bf16_hi(v[u].z), c, -mc)) + ex2(fmaf(bf16_hi(v[u].w), c, -mc));
+                const float x[VEC] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
+                                      bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
+                exp2_sum8(x, c, mc, a0, a1);
             }
         }
     }
-    acc.s = s0 + s1;
+    acc.s = (a0.x + a0.y) + (a1.x + a1.y);
     return acc;
 }
 
@@ -300,32 +297,36 @@ struct StagedP {  // w = p = 2^((l - m) c) / S
     __device__ __forceinline__ void eval8(int e0, int hi, float w[VEC]) const {
         float l[VEC];
         smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
-        const float mc = m * c;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) w[j] = ex2(fmaf(l[j], c, -mc)) * inv_s;
+        exp2_scale8(l, c, m * c, inv_s, w);
     }
 };
+
+// w_j = max(0, p_j - q_j) from eight probabilities of each (exact subtraction, no contraction).
+__device__ __forceinline__ void residual8(const float p[VEC], const float q[VEC], float w[VEC]) {
+#pragma unroll
+    for (int j = 0; j < VEC; j += 2) {
+        const float2 r = fadd2(make_float2(p[j], p[j + 1]), make_float2(-q[j], -q[j + 1]));
+        w[j] = fmaxf(r.x, 0.f);
+        w[j + 1] = fmaxf(r.y, 0.f);
+    }
+}
 
 // w = max(0, p - q) with the target chunk staged and the draft-logit row read from
 // global memory (it was streamed for its statistics just before, so from L2).
 template <int TDT, int DDT>
 struct StagedResidualD {
-    static constexpr int kTilesInFlight = 2;  // global loads: two tiles in flight per warp
+    static constexpr int kTilesInFlight = 4;  // global loads: several tiles in flight per warp
     const unsigned char* tb;
     const void* drow;
     int lo;
     float c, mt, inv_st, md, inv_sd;
     __device__ __forceinline__ void eval8(int e0, int hi, float w[VEC]) const {
-        float l[VEC], d[VEC];
+        float l[VEC], d[VEC], p[VEC], q[VEC];
         smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
         load8<DDT>(drow, e0, hi, true, neg_inf(), d);
-        const float mtc = mt * c, mdc = md * c;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-            const float p = ex2(fmaf(l[j], c, -mtc)) * inv_st;
-            const float q = ex2(fmaf(d[j], c, -mdc)) * inv_sd;
-            w[j] = fmaxf(p - q, 0.f);
-        }
+        exp2_scale8(l, c, mt * c, inv_st, p);
+        exp2_scale8(d, c, md * c, inv_sd, q);
+        residual8(p, q, w);
     }
 };
 
@@ -336,15 +337,16 @@ struct StagedResidual {  // w = max(0, p - q)
     int lo;
     float c, mt, inv_st, md, inv_sd;
     __device__ __forceinline__ void eval8(int e0, int hi, float w[VEC]) const {
-        float l[VEC], d[VEC];
+        float l[VEC], d[VEC], p[VEC];
         smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
         smem_load8<DDT>(db, e0 - lo, hi - lo, DK == DK_LOGITS ? neg_inf() : 0.f, d);
-        const float mtc = mt * c, mdc = md * c;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-            const float p = ex2(fmaf(l[j], c, -mtc)) * inv_st;
-            const float q = (DK == DK_LOGITS) ? ex2(fmaf(d[j], c, -mdc)) * inv_sd : d[j];
-            w[j] = fmaxf(p - q, 0.f);
+        exp2_scale8(l, c, mt * c, inv_st, p);
+        if (DK == DK_LOGITS) {
+            float q[VEC];
+            exp2_scale8(d, c, md * c, inv_sd, q);
+            residual8(p, q, w);
+        } else {
+            residual8(p, d, w);
         }
     }
 };
