@@ -229,8 +229,10 @@ __global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
         }
     }
     // a copy still in flight must land before the CTA exits (a greedy or invalid row
-    // never waited for its q chunk)
-    if (!draft_landed && threadIdx.x == 0) (void)mbar_wait_bounded(dbar, 0);
+    // never waited for its q chunk); if that bounded wait gives up, the reporting CTA
+    // marks the position invalid (another CTA's failed drain is not seen by the reporter)
+    int drain_bad = 0;
+    if (!draft_landed && threadIdx.x == 0) drain_bad = mbar_wait_bounded(dbar, 0) ? 0 : 1;
     // 4. one CTA reports the position (all of them know its outcome): the owner of the
     // drawn token when there is a draw, else rank 0.  It writes output slot k (the kept
     // draft, the greedy row's argmax or the drawn token) and the acceptance probability,
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
         }
         unsigned long long inc = 1ull;
         if (k < K && !accept) inc |= 1ull << (SPEC_REJ_SHIFT + k);
-        if (bad) inc |= 1ull << (SPEC_BAD_SHIFT + k);
+        if (bad || drain_bad) inc |= 1ull << (SPEC_BAD_SHIFT + k);
         unsigned long long* word = reinterpret_cast<unsigned long long*>(A.ws + A.wl.counter_off) + b;
         const unsigned long long old = atomic_add_acq_rel(word, inc);  // releases the slot just written
         s_word = old + inc;

@@ -246,10 +246,12 @@ __global__ void __launch_bounds__(NT, 4) chain_staged_kernel(const ChainArgs a, 
         writer = d.owner;
         break;
     }
-    // copies still in flight (prefetched positions never reached) must land before the CTA exits
+    // copies still in flight (prefetched positions never reached) must land before the CTA
+    // exits; a wait that gives up here reports the row as timed out
+    int drain_fail = 0;
     for (int s = 0; s < L.nslot; ++s)
-        if ((tpend | dpend) & (1u << s)) (void)wait_slot(s);
-    __syncthreads();
+        if ((tpend | dpend) & (1u << s)) drain_fail |= wait_slot(s) ? 0 : 1;
+    if (__syncthreads_or(drain_fail)) tmo = 1;
     if (invalid) writer = 0;
     if (g == writer) {
         int32_t* ot = a.out_tokens + (size_t)b * (K + 1);

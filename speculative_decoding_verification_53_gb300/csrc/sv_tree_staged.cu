@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
     complete_issue(0, 0, with_draft);
     bool invalid = __syncthreads_or(bad) != 0;
     int tmo = 0;  // some wait of the row gave up (this CTA's, or a peer's flag seen in an exchange)
+    int drain_fail = 0;  // a wait for a copy that was not used gave up (this thread)
     if (!invalid) {
         // every node's depth must fit max_depth: depths by pointer jumping on (count, target)
         // pairs, read / barrier / write rounds; a node stops at the root or beyond D
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
             for (int t = 0; t < L.nslot; ++t)
                 if (slot_row[t] < 0) { s = t; break; }
             if (s < 0) break;
-            if (pend & (1u << s)) (void)wait_slot(s);  // a dropped prefetch still in flight
+            if (pend & (1u << s)) drain_fail |= wait_slot(s) ? 0 : 1;  // a dropped prefetch still in flight
             const int crow = s_child[q] + 1;
             __syncthreads();
             issue_t(crow, s);
@@ -419,7 +420,7 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
         __syncthreads();  // every read of the previous node's slot is done
         if (s_next < 0) {
             s_next = s_cur;
-            if (pend & (1u << s_next)) (void)wait_slot(s_next);
+            if (pend & (1u << s_next)) drain_fail |= wait_slot(s_next) ? 0 : 1;
             issue_t(next + 1, s_next);
             complete_issue(next + 1, s_next, with_draft);
             pend |= 1u << s_next;
@@ -428,8 +429,10 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
         s_cur = s_next;
     }
     for (int s = 0; s < L.nslot; ++s)  // copies in flight must land before the CTA exits
-        if (pend & (1u << s)) (void)wait_slot(s);
-    __syncthreads();
+        if (pend & (1u << s)) drain_fail |= wait_slot(s) ? 0 : 1;
+    // a wait for a copy that was not used (a dropped prefetch) that gave up: the slot may
+    // still have been written after it was reused, so the row reports a timeout
+    if (__syncthreads_or(drain_fail)) tmo = 1;
     if (invalid) writer = 0;
     if (g == writer) {
         int32_t* ot = a.out_tokens + (size_t)b * (D + 1);
