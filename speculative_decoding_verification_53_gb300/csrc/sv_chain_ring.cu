@@ -17,6 +17,12 @@
 // hundred resident, so while some rows exchange statistics, draw or wait for a
 // decision, the others keep their bulk copies in flight.
 //
+// Measured, this loses to the staged walk (B = 256, K = 8, V = 152064: 212 against
+// 146 us at T = 0.7): a CTA of four warps alone on its SM streams and reduces only
+// about 10 GB/s, so once most rows have finished, the long chains that remain crawl.
+// It runs only when requested (SPEC_VERIFY_PATH=ring) and is kept, tested, as the
+// record of that design.
+//
 // Per position k, every CTA streams its chunk [lo, hi) of the target row (and of the
 // draft-logit row) through the ring, reducing online to (max, sum of exp2) per row
 // (greedy rows: the argmax); the cluster combines the partials through distributed
@@ -38,16 +44,6 @@ constexpr int RING_TPW = RING_TILES / RING_NW;  // tiles per warp per stage
 constexpr int RING_MAX_G = 8;
 constexpr int RING_HEADER = 128;        // the stages' mbarriers
 static_assert(RING_TILES % RING_NW == 0, "whole tiles per warp");
-
-// L2 held by the rows' prefetch windows (bytes announced but not yet streamed), shared by
-// every row that is walking.
-constexpr uint32_t RING_L2_BUDGET = 48u << 20;
-
-// Rows of ring launches that are walking right now on this device: each row adds 1 when it
-// starts and takes it back when it ends.  Only a heuristic reads it -- the depth of the
-// L2 prefetch window -- so launches on other streams that share it change speed, never
-// results.
-__device__ unsigned int g_ring_active_rows;
 
 // Exchange state of a ring CTA (the fields the draw's exchange in sv_common.cuh uses,
 // sized for four warps).
@@ -241,7 +237,6 @@ __global__ void __launch_bounds__(RING_NT, 8) chain_ring_kernel(const ChainArgs 
     const bool greedy = !(T > 0.f);
     const float c = greedy ? 0.f : LOG2E / T;
     const bool draft_rows = !greedy && DK == DK_LOGITS;  // draft-logit rows are streamed with the target rows
-    if (g == 0 && threadIdx.x == 0) atomicAdd(&g_ring_active_rows, 1u);
 
     // Ring bookkeeping: stage number gs (counted over the whole kernel) lives in slot
     // gs % nstage and completes phase (gs / nstage) of that slot's barrier.  A pass over
@@ -258,33 +253,9 @@ __global__ void __launch_bounds__(RING_NT, 8) chain_ring_kernel(const ChainArgs 
         bulk_g2s(st, tbase + ((size_t)k * V + e0) * tsz, (uint32_t)cnt * tsz, &full[s]);
         if (with_d) bulk_g2s(st + L.t_bytes, dbase + ((size_t)k * V + e0) * dsz, (uint32_t)cnt * dsz, &full[s]);
     };
-    // L2 prefetch window (thread 0 only): pieces [nstage, pf) of the current pass have
-    // been announced to L2 with cp.async.bulk.prefetch, so that when their ring copy is
-    // issued they come from L2.  The window is wide when few rows are walking (a long
-    // chain at the end of the batch then streams near an SM's full rate) and narrow when
-    // many are (their windows together stay within RING_L2_BUDGET).
-    int pf = 0, pwin = 0;
-    auto prefetch_to = [&](int k, bool with_d, int upto) {
-        for (; pf < upto; ++pf) {
-            const int e0 = lo + pf * RING_PE;
-            const int cnt = min(RING_PE, hi - e0);
-            prefetch_l2(tbase + ((size_t)k * V + e0) * tsz, (uint32_t)cnt * tsz);
-            if (with_d) prefetch_l2(dbase + ((size_t)k * V + e0) * dsz, (uint32_t)cnt * dsz);
-        }
-    };
     auto issue_first = [&](int k, bool with_d) {
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 0)
             for (int j = 0; j < L.nstage && j < npieces; ++j) issue(k, with_d, j, gs + (uint32_t)j);
-            // (position 0: every row of the launch is about to stream, whether or not it has
-            // counted itself in yet)
-            unsigned rows = *reinterpret_cast<volatile unsigned*>(&g_ring_active_rows);
-            if (k == 0 && rows < (unsigned)a.B) rows = (unsigned)a.B;
-            const uint32_t piece = (uint32_t)RING_PE * (tsz + (with_d ? dsz : 0));
-            const uint32_t per_cta = RING_L2_BUDGET / ((rows ? rows : 1u) * (uint32_t)G);
-            pwin = (int)min((uint32_t)npieces, per_cta / piece);
-            pf = L.nstage;
-            prefetch_to(k, with_d, min(npieces, L.nstage + pwin));
-        }
     };
     // Waits for piece j of the current pass and returns its stage; `fail` collects waits
     // that gave up.
@@ -294,14 +265,10 @@ __global__ void __launch_bounds__(RING_NT, 8) chain_ring_kernel(const ChainArgs 
         if (!mbar_wait_bounded(&full[s], (gsj / (uint32_t)L.nstage) & 1u)) fail = 1;
         return stages + (size_t)s * L.stage_bytes;
     };
-    // After piece j has been read by every thread: refill its slot with piece j + nstage,
-    // and move the prefetch window along.
+    // After piece j has been read by every thread: refill its slot with piece j + nstage.
     auto release_piece = [&](int k, bool with_d, int j) {
         __syncthreads();
-        if (threadIdx.x == 0 && j + L.nstage < npieces) {
-            issue(k, with_d, j + L.nstage, gs + (uint32_t)(j + L.nstage));
-            prefetch_to(k, with_d, min(npieces, j + 1 + L.nstage + pwin));
-        }
+        if (threadIdx.x == 0 && j + L.nstage < npieces) issue(k, with_d, j + L.nstage, gs + (uint32_t)(j + L.nstage));
     };
 
     issue_first(0, draft_rows && K > 0);  // position 0 goes out before the token checks
@@ -524,7 +491,6 @@ __global__ void __launch_bounds__(RING_NT, 8) chain_ring_kernel(const ChainArgs 
     // saw a timeout then marks the row (after the barrier, so after any other writer).
     cluster_sync_all();
     if (tmo && threadIdx.x == 0) a.out_count[b] = SV_COUNT_TIMEOUT;
-    if (g == 0 && threadIdx.x == 0) atomicSub(&g_ring_active_rows, 1u);
 }
 
 size_t ring_smem_bytes(const RingLayout& L, int V, int G) {

@@ -178,9 +178,12 @@ __global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
         accept = k < K && x == am.i;
         amax = am.i;
     } else {
-        LSE ts = smem_thread_lse<TDT>(tb, n, c);
-        LSE ds{neg_inf(), 0.f, 0};
-        if (DK == DK_LOGITS && k < K) ds = smem_thread_lse<DDT>(db, n, c);
+        LSE ts, ds{neg_inf(), 0.f, 0};
+        if (DK == DK_LOGITS && k < K) {
+            smem_thread_lse2<TDT, DDT>(tb, db, n, c, ts, ds);
+        } else {
+            ts = smem_thread_lse<TDT>(tb, n, c);
+        }
         if (fail) ts.bad = 1;
         float tx = 0.f, dx = 0.f;
         int has = 0;

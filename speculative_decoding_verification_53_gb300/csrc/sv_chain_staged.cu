@@ -174,9 +174,13 @@ __global__ void __launch_bounds__(NT, 4) chain_staged_kernel(const ChainArgs a, 
             writer = 0;
             break;
         }
-        LSE ts = smem_thread_lse<TDT>(tb, n, c);
-        LSE ds{neg_inf(), 0.f, 0};
-        if (draft_rows && k < K) ds = d_direct ? ds_direct : smem_thread_lse<DDT>(db, n, c);
+        LSE ts, ds{neg_inf(), 0.f, 0};
+        if (draft_rows && k < K && !d_direct) {
+            smem_thread_lse2<TDT, DDT>(tb, db, n, c, ts, ds);
+        } else {
+            ts = smem_thread_lse<TDT>(tb, n, c);
+            if (draft_rows && k < K) ds = ds_direct;
+        }
         if (fail) ts.bad |= BAD_TIMEOUT;
         float tx = 0.f, dx = 0.f;
         int has = 0;

@@ -101,6 +101,34 @@ __device__ __forceinline__ LSE smem_thread_lse(const unsigned char* buf, int n, 
     return acc;
 }
 
+// smem_thread_lse of a target chunk and a draft-logit chunk at once: the two maxima, then
+// one loop over both chunks (twice the independent exponentials per iteration, which
+// helps a CTA that is alone on its SM).
+template <int TDT, int DDT>
+__device__ __forceinline__ void smem_thread_lse2(const unsigned char* tb, const unsigned char* db, int n, float c,
+                                                 LSE& t, LSE& d) {
+    const float mt = smem_thread_max<TDT>(tb, n), md = smem_thread_max<DDT>(db, n);
+    t = LSE{mt, 0.f, mt != mt ? 1 : 0};
+    d = LSE{md, 0.f, md != md ? 1 : 0};
+    const bool use_t = mt > neg_inf() && !t.bad, use_d = md > neg_inf() && !d.bad;
+    if (!use_t || !use_d) {  // a degenerate chunk: the single-row loops
+        if (use_t) t = smem_thread_lse<TDT>(tb, n, c);
+        if (use_d) d = smem_thread_lse<DDT>(db, n, c);
+        return;
+    }
+    const float mtc = mt * c, mdc = md * c;
+    float2 t0 = make_float2(0.f, 0.f), t1 = t0, d0 = t0, d1 = t0;
+    for (int e = (int)threadIdx.x * VEC; e < n; e += NT * VEC) {
+        float x[VEC], y[VEC];
+        smem_load8<TDT>(tb, e, n, neg_inf(), x);
+        smem_load8<DDT>(db, e, n, neg_inf(), y);
+        exp2_sum8(x, c, mtc, t0, t1);
+        exp2_sum8(y, c, mdc, d0, d1);
+    }
+    t.s = (t0.x + t0.y) + (t1.x + t1.y);
+    d.s = (d0.x + d0.y) + (d1.x + d1.y);
+}
+
 // (max, sum 2^((l - max) c)) of one thread's share of elements [lo, hi) of a row in global
 // memory (16-byte aligned; lo a multiple of 8), online: four 16-byte vectors in flight per
 // thread, kept packed until used (bf16 rows: the maximum of a vector by max.bf16x2, no

@@ -152,6 +152,13 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
                             &bars[s]);
         }
     };
+    auto issue_t_nofence = [&](int row, int s) {  // issue_t after the caller's proxy fence
+        if (threadIdx.x == 0) {
+            mbar_expect_tx(&bars[s], (uint32_t)n * tsz);
+            if (n) bulk_g2s(slots + (size_t)s * L.slot_bytes, tbase + ((size_t)row * V + lo) * tsz, (uint32_t)n * tsz,
+                            &bars[s]);
+        }
+    };
     auto complete_issue = [&](int row, int s, bool with_draft) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(&bars[s], with_draft ? (uint32_t)n * dsz : 0u);
@@ -247,19 +254,30 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
         __syncthreads();
         const int nchild = s_nchild;
         // prefetch the children's rows into free slots (before the gathers below: the proxy
-        // fence of a copy would otherwise wait for thread 0's outstanding loads)
-        for (int q = 0; q < nchild; ++q) {
-            int s = -1;
-            for (int t = 0; t < L.nslot; ++t)
-                if (slot_row[t] < 0) { s = t; break; }
-            if (s < 0) break;
-            if (pend & (1u << s)) drain_fail |= wait_slot(s) ? 0 : 1;  // a dropped prefetch still in flight
-            const int crow = s_child[q] + 1;
-            __syncthreads();
-            issue_t(crow, s);
-            complete_issue(crow, s, with_draft);
-            slot_row[s] = crow;
-            pend |= 1u << s;
+        // fence of a copy would otherwise wait for thread 0's outstanding loads).  A free
+        // slot's reads ended at the barrier the walk passed when it descended; a dropped
+        // prefetch still in flight is waited for by every thread first.  Then one barrier
+        // and one proxy fence cover the whole batch of copies.
+        {
+            int sq[16], nq = 0;
+            for (int q = 0; q < nchild && nq < 16; ++q) {
+                int s = -1;
+                for (int t = 0; t < L.nslot; ++t)
+                    if (slot_row[t] < 0) { s = t; break; }
+                if (s < 0) break;
+                if (pend & (1u << s)) drain_fail |= wait_slot(s) ? 0 : 1;  // a dropped prefetch still in flight
+                slot_row[s] = s_child[q] + 1;
+                pend |= 1u << s;
+                sq[nq++] = s;
+            }
+            if (nq > 0) {
+                __syncthreads();
+                if (threadIdx.x == 0) fence_proxy_async();
+                for (int i = 0; i < nq; ++i) {
+                    issue_t_nofence(slot_row[sq[i]], sq[i]);
+                    complete_issue(slot_row[sq[i]], sq[i], with_draft);
+                }
+            }
         }
         // raw values of the children's tokens in this node's rows (sampling): the loads are
         // issued now and their values stored after the statistics, so the latency overlaps
@@ -285,9 +303,12 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
             if (threadIdx.x == 0) s_out[emitted] = am.i;
             if (next < 0) { ++emitted; writer = 0; break; }
         } else {
-            LSE ts = smem_thread_lse<TDT>(tb, n, c);
-            LSE ds{neg_inf(), 0.f, 0};
-            if (DK == DK_LOGITS && nchild > 0) ds = smem_thread_lse<DDT>(db, n, c);
+            LSE ts, ds{neg_inf(), 0.f, 0};
+            if (DK == DK_LOGITS && nchild > 0) {
+                smem_thread_lse2<TDT, DDT>(tb, db, n, c, ts, ds);
+            } else {
+                ts = smem_thread_lse<TDT>(tb, n, c);
+            }
             if (fail) ts.bad |= BAD_TIMEOUT;
             if (gat) {
                 s_rt[threadIdx.x] = g_rt;
