@@ -131,13 +131,17 @@ __global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
     }
     pdl_trigger();
     pdl_wait();  // nothing the previous kernel on the stream writes is read before this
+    // The draft chunk goes out with the target chunk when the statistics need it (draft
+    // logits); draft probabilities are needed by the draw alone, so their chunk is copied
+    // once the target chunk has landed and does not share the SM's copy bandwidth with it.
+    auto issue_draft = [&]() {
+        mbar_arrive_expect_tx(dbar, (uint32_t)n * dsz);
+        if (n) bulk_g2s(db, drow + (size_t)lo * dsz, (uint32_t)n * dsz, dbar);
+    };
     if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(tbar, (uint32_t)n * tsz);
         if (n) bulk_g2s(tb, trow + (size_t)lo * tsz, (uint32_t)n * tsz, tbar);
-        if (has_draft_row) {
-            mbar_arrive_expect_tx(dbar, (uint32_t)n * dsz);
-            if (n) bulk_g2s(db, drow + (size_t)lo * dsz, (uint32_t)n * dsz, dbar);
-        }
+        if (has_draft_row && DK == DK_LOGITS) issue_draft();
     }
     // draft probabilities: only q(x_k) takes part in the statistics, so thread 0 fetches
     // it directly and the q chunk (needed by the draw alone) keeps landing meanwhile
@@ -159,7 +163,10 @@ __global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
 
     // 2. statistics of row k, the acceptance test of x_k
     bool ok = mbar_wait_bounded(tbar, 0);
-    bool draft_landed = !has_draft_row;
+    // (a greedy row never draws: its probability chunk is not copied at all)
+    const bool probs_copied = has_draft_row && DK == DK_PROBS && !greedy;
+    if (probs_copied && threadIdx.x == 0) issue_draft();
+    bool draft_landed = !has_draft_row || (DK == DK_PROBS && !probs_copied);
     if (has_draft_row && DK == DK_LOGITS) {  // draft logits feed the statistics
         ok = mbar_wait_bounded(dbar, 0) && ok;
         draft_landed = true;
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
     float ratio = 0.f;
     if (greedy) {
         ArgMax am = smem_thread_argmax<TDT>(tb, n, lo);
-        if (fail) am.bad = 1;
+        if (fail) am.bad |= BAD_TIMEOUT;
         am = cluster_argmax(am, sc, phase);
         bad = am.bad || !(am.v > neg_inf()) || am.v == pos_inf();
         accept = k < K && x == am.i;
@@ -184,7 +191,7 @@ __global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
         } else {
             ts = smem_thread_lse<TDT>(tb, n, c);
         }
-        if (fail) ts.bad = 1;
+        if (fail) ts.bad |= BAD_TIMEOUT;
         float tx = 0.f, dx = 0.f;
         int has = 0;
         if (threadIdx.x == 0 && x >= lo && x < hi) {
