@@ -329,6 +329,10 @@ class Timed:
             ws_bytes = sv.spec_verify_workspace_size(rows, K_, w["target"].shape[2])
             ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=device)
         n_inputs = self.n_inputs
+        # every tensor the captured graphs read or write stays referenced by this object:
+        # a graph holds raw device pointers only, so a tensor that went out of scope here
+        # would be freed and its memory reused while the graphs still run on it
+        self._graph_tensors = [dt, dd, dtok, dtemp, out_t] + ([dpar, self.out_p] if self.tree else [out_x, ws])
 
         def step(i, slot):
             r = (i % n_inputs) * rows
@@ -401,6 +405,8 @@ class Timed:
         w, rows = self.w, self.w["per_step_rows"]
         n = self.chunk if self.reps else self.rem
         counts = self.out_c[:n].cpu().numpy()
+        if not (counts >= 1).all():  # the synthetic workloads hold no invalid rows
+            raise RuntimeError(f"{int((counts < 1).sum())} rows of the timed steps are not valid")
         alg, dense = [], []
         for s in range(n):
             r = (s % self.n_inputs) * rows
@@ -567,9 +573,9 @@ def workload_config(w, world):
             "parallelism": f"replicas x{world}"}
 
 
-def _packed(arrays, device):
+def _packed(arrays, device, copies=1):
     """One pinned host buffer holding the arrays back to back (16-byte aligned offsets),
-    a device buffer of the same size, and device views of each array in it."""
+    `copies` device buffers of the same size, and device views of each array in each."""
     import torch
     parts, off = [], 0
     for a in arrays:
@@ -578,13 +584,18 @@ def _packed(arrays, device):
         off += (a.nbytes + 15) // 16 * 16
     host = torch.zeros(off, dtype=torch.uint8).pin_memory()
     hv = host.numpy()
-    dev = torch.empty(off, dtype=torch.uint8, device=device)
-    views = []
     for o, a in parts:
         hv[o:o + a.nbytes] = np.frombuffer(a.tobytes(), dtype=np.uint8)
-        dt = torch.bfloat16 if a.dtype == np.uint16 else getattr(torch, a.dtype.name)
-        views.append(dev[o:o + a.nbytes].view(dt).view(a.shape))
-    return host, dev, views
+    devs, views = [], []
+    for _ in range(copies):
+        dev = torch.empty(off, dtype=torch.uint8, device=device)
+        v = []
+        for o, a in parts:
+            dt = torch.bfloat16 if a.dtype == np.uint16 else getattr(torch, a.dtype.name)
+            v.append(dev[o:o + a.nbytes].view(dt).view(a.shape))
+        devs.append(dev)
+        views.append(v)
+    return host, devs, views
 
 
 def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
@@ -606,7 +617,8 @@ def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
     else:
         names = ["target", "draft", "tokens", "temperature"]
         out_cols = w["tokens"].shape[1] + 1
-    hin, din, views = _packed([w[k][sl] for k in names], device)
+    hin, dins, vs = _packed([w[k][sl] for k in names], device)
+    din, views = dins[0], vs[0]
     # outputs back to back in one device buffer: tokens [B][cols], count [B] (and the
     # tree's path, not read back)
     dout = torch.empty(per_step_rows * (out_cols + 1), dtype=torch.int32, device=device)
@@ -652,6 +664,8 @@ def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
         got = v.cpu().view(torch.int16).numpy().view(np.uint16) if a.dtype == np.uint16 else v.cpu().numpy()
         if not np.array_equal(got.view(np.uint8), a.view(np.uint8)):
             raise RuntimeError(f"end-to-end staging of {k} is wrong")
+    if not (hout[per_step_rows * out_cols:] >= 1).all():  # every row of the last step verified
+        raise RuntimeError("end-to-end counts are not all valid")
     return {"value": per_step_rows * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(hin.numel()),
             "d2h_bytes_per_step": int(hout.numel() * 4), "steps": n, "ms_per_step": ms / n,
             "staging": "inputs packed in one pinned buffer (one copy in), tokens and counts in one (one copy out)"}
