@@ -162,13 +162,14 @@ __global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
     const bool tokens_bad = __syncthreads_or(tok_bad) != 0;
 
     // 2. statistics of row k, the acceptance test of x_k
-    bool ok = mbar_wait_bounded(tbar, 0);
+    // thread 0 polls the copy barriers; the CTA barrier below releases the other threads
+    bool ok = threadIdx.x != 0 || mbar_wait_bounded(tbar, 0);
     // (a greedy row never draws: its probability chunk is not copied at all)
     const bool probs_copied = has_draft_row && DK == DK_PROBS && !greedy;
     if (probs_copied && threadIdx.x == 0) issue_draft();
     bool draft_landed = !has_draft_row || (DK == DK_PROBS && !probs_copied);
     if (has_draft_row && DK == DK_LOGITS) {  // draft logits feed the statistics
-        ok = mbar_wait_bounded(dbar, 0) && ok;
+        ok = (threadIdx.x != 0 || mbar_wait_bounded(dbar, 0)) && ok;
         draft_landed = true;
     }
     const int fail = __syncthreads_or(!ok);
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(NT, 1) chain_spec_kernel(const SpecArgs A) {
             if (k < K) {
                 int dfail = 0;
                 if (!draft_landed) {  // the q chunk, for the residual
-                    dfail = __syncthreads_or(!mbar_wait_bounded(dbar, 0));
+                    dfail = __syncthreads_or(threadIdx.x == 0 && !mbar_wait_bounded(dbar, 0));
                     draft_landed = true;
                 }
                 // one CTA per SM here: four tiles in flight per warp shorten the draw's

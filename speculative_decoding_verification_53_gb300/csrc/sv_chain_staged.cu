@@ -125,15 +125,18 @@ __global__ void __launch_bounds__(NT, 4) chain_staged_kernel(const ChainArgs a, 
         tpend |= 1u << s;
         if (copy_d && k < K) dpend |= 1u << s;
     };
-    auto wait_slot = [&](int s) -> bool {  // both chunks of slot s (the draft one only if requested)
+    // Both chunks of slot s (the draft one only if requested).  Thread 0 polls the
+    // barriers; every call is followed by a CTA barrier, which carries its observation of
+    // the landed copies to the other threads (they wait there without taking issue slots).
+    auto wait_slot = [&](int s) -> bool {
         bool ok = true;
         if (tpend & (1u << s)) {
-            ok = mbar_wait_bounded_ns(&tbar[s], (tpar >> s) & 1u, wait_ns);
+            if (threadIdx.x == 0) ok = mbar_wait_bounded_ns(&tbar[s], (tpar >> s) & 1u, wait_ns);
             tpar ^= 1u << s;
             tpend &= ~(1u << s);
         }
         if (dpend & (1u << s)) {
-            ok = mbar_wait_bounded(&dbar[s], (dpar >> s) & 1u) && ok;
+            if (threadIdx.x == 0) ok = mbar_wait_bounded(&dbar[s], (dpar >> s) & 1u) && ok;
             dpar ^= 1u << s;
             dpend &= ~(1u << s);
         }
@@ -228,12 +231,12 @@ __global__ void __launch_bounds__(NT, 4) chain_staged_kernel(const ChainArgs a, 
             } else if (threadIdx.x == 0) {
                 mbar_arrive_expect_tx(pbar, 0u);
             }
-            dfail = __syncthreads_or(!mbar_wait_bounded(pbar, 0u));
+            dfail = __syncthreads_or(threadIdx.x == 0 && !mbar_wait_bounded(pbar, 0u));
             qb = probs_area;
         }
         DrawResult d;
         if (d_direct) {
-            const StagedResidualD<TDT, DDT> rw{tb, drow, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd};
+            const StagedResidualD<TDT, DDT> rw{tb, drow, lo, c, ps.t.m, ps.d.m, ps.t.s / ps.d.s};
             d = cluster_draw(rw, lo, hi, s_u[k], tile_sum, sc, phase, dfail);
         } else {
             const StagedResidual<TDT, DDT, DK> rw{tb, qb, lo, c, ps.t.m, inv_st, ps.d.m, inv_sd};

@@ -57,6 +57,15 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     return d;
 }
 
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
     float2 d;
     asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
@@ -64,6 +73,14 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
+}
+
+// Sum of eight values, pairwise on the packed two-lane adder.
+__device__ __forceinline__ float sum8(const float w[8]) {
+    const float2 a = fadd2(make_float2(w[0], w[1]), make_float2(w[2], w[3]));
+    const float2 b = fadd2(make_float2(w[4], w[5]), make_float2(w[6], w[7]));
+    const float2 t = fadd2(a, b);
+    return t.x + t.y;
 }
 
 // Sum of 2^(x_j c - mc) over eight values, as two packed accumulators.
@@ -827,9 +844,7 @@ __device__ __forceinline__ DrawResult cluster_draw_from_tiles(const WF& wf, int 
             const int e0 = lo + tile * TILE + lane * VEC;
             float w[VEC];
             wf.eval8(e0, hi, w);
-            float ls = 0.f;
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) ls += w[j];
+            const float ls = sum8(w);
             float incl = ls;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -869,6 +884,39 @@ __device__ __forceinline__ DrawResult cluster_draw_from_tiles(const WF& wf, int 
     return res;
 }
 
+// Warp totals of TB per-lane values (TB = 1, 2 or 4), written to tile_sum[t0 + i] for the
+// tiles below ntiles.  For TB > 1 the values are reduced transposed: each exchange step
+// halves the values a lane keeps, so TB totals take TB - 1 + 5 - log2(TB) shuffles instead
+// of 5 TB.
+template <int TB>
+__device__ __forceinline__ void warp_tile_sums(const float s[TB], int lane, int t0, int ntiles, float* tile_sum) {
+    static_assert(TB == 1 || TB == 2 || TB == 4, "tiles in flight: 1, 2 or 4");
+    float k;
+    int i;
+    if (TB == 1) {
+        k = s[0];
+        i = 0;
+    } else if (TB == 2) {
+        const bool b16 = (lane & 16) != 0;
+        k = (b16 ? s[TB - 1] : s[0]) + __shfl_xor_sync(0xffffffffu, b16 ? s[0] : s[TB - 1], 16);
+        i = b16 ? 1 : 0;
+    } else {
+        const bool b16 = (lane & 16) != 0, b8 = (lane & 8) != 0;
+        // lanes without bit 4 of the lane index set keep tiles 0 and 1, the others 2 and 3
+        float k0 = b16 ? s[2 % TB] : s[0], k1 = b16 ? s[3 % TB] : s[1 % TB];
+        k0 += __shfl_xor_sync(0xffffffffu, b16 ? s[0] : s[2 % TB], 16);
+        k1 += __shfl_xor_sync(0xffffffffu, b16 ? s[1 % TB] : s[3 % TB], 16);
+        // then lanes without bit 3 keep the even tile of their pair, the others the odd one
+        k = (b8 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b8 ? k0 : k1, 8);
+        i = (b16 ? 2 : 0) + (b8 ? 1 : 0);
+    }
+    // the lanes sharing a tile differ in the remaining low bits
+#pragma unroll
+    for (int o = (TB == 1 ? 16 : (TB == 2 ? 8 : 4)); o > 0; o >>= 1) k += __shfl_xor_sync(0xffffffffu, k, o);
+    const int width = 32 / TB;  // lanes per tile after the transposed steps
+    if (lane % width == 0 && t0 + i < ntiles) tile_sum[t0 + i] = k;
+}
+
 // Tiles a warp evaluates before reducing them: weight functors that read global memory
 // declare kTilesInFlight (several loads in flight per lane); shared-memory ones take 1.
 template <class T, class = void>
@@ -879,6 +927,28 @@ template <class T>
 struct TilesInFlight<T, decltype((void)T::kTilesInFlight)> {
     static constexpr int value = T::kTilesInFlight;
 };
+
+// Weight functors whose eval8_full(e0, w) evaluates eight elements that all lie below the
+// end of the range (no bounds tests) use it for the draw's full tiles.
+template <class T, class = void>
+struct HasFullEval {
+    static constexpr bool value = false;
+};
+template <class T>
+struct HasFullEval<T, decltype((void)&T::eval8_full)> {
+    static constexpr bool value = true;
+};
+
+template <class WF>
+__device__ __forceinline__ void eval8_any(const WF& wf, int e0, int hi, bool full, float w[VEC]) {
+    if constexpr (HasFullEval<WF>::value) {
+        if (full) {
+            wf.eval8_full(e0, w);
+            return;
+        }
+    }
+    wf.eval8(e0, hi, w);
+}
 
 // A weight functor with TB tiles in flight per warp, for kernels whose draw is bound by
 // latency rather than by the exp2 pipe (one CTA per SM).
@@ -894,26 +964,20 @@ __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float*
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nw = (int)(blockDim.x >> 5);  // warps of this CTA
     const int ntiles = (hi - lo + TILE - 1) / TILE;
+    const int nfull = (hi - lo) / TILE;  // tiles with no element at or beyond hi
     for (int t0 = warp * TB; t0 < ntiles; t0 += nw * TB) {
-        float w[TB][VEC];
+        float s[TB];  // each tile's weights are summed as soon as they are evaluated
+        const bool full = t0 + TB <= nfull;
 #pragma unroll
         for (int i = 0; i < TB; ++i) {
+            s[i] = 0.f;
             if (t0 + i < ntiles) {
-                wf.eval8(lo + (t0 + i) * TILE + lane * VEC, hi, w[i]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) w[i][j] = 0.f;
+                float w[VEC];
+                eval8_any(wf, lo + (t0 + i) * TILE + lane * VEC, hi, full, w);
+                s[i] = sum8(w);
             }
         }
-#pragma unroll
-        for (int i = 0; i < TB; ++i) {
-            float s = 0.f;
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) s += w[i][j];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0 && t0 + i < ntiles) tile_sum[t0 + i] = s;
-        }
+        warp_tile_sums<TB>(s, lane, t0, ntiles, tile_sum);
     }
     __syncthreads();
     return cluster_draw_from_tiles(wf, lo, hi, u, tile_sum, sc, phase, fail_in);

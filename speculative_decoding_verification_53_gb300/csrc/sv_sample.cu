@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(NT) draft_sample_staged_kernel(const SampleArg
     const bool greedy = !(T > 0.f);
     int32_t* out = a.out_draft_tokens + (size_t)b * a.K + k;
     __syncthreads();  // the barrier is initialised (by thread 0) before anyone polls it
-    const int fail = __syncthreads_or(!mbar_wait_bounded(bar, 0));
+    const int fail = __syncthreads_or(threadIdx.x == 0 && !mbar_wait_bounded(bar, 0));  // thread 0 polls
     int phase = 0;
     if (greedy) {
         ArgMax am = smem_thread_argmax<DDT>(db, n, lo);

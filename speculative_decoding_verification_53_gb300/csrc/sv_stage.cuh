@@ -42,6 +42,21 @@ __device__ __forceinline__ void smem_load8(const unsigned char* buf, int e, int 
     }
 }
 
+// Eight staged elements e..e+7, all below the chunk's end (no bounds test).
+template <int DT>
+__device__ __forceinline__ void smem_load8_full(const unsigned char* buf, int e, float x[VEC]) {
+    if (DT == DT_BF16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(buf + (size_t)e * 2);
+        x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+        x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+    } else {
+        const float4 a = *reinterpret_cast<const float4*>(buf + (size_t)e * 4);
+        const float4 b = *reinterpret_cast<const float4*>(buf + (size_t)e * 4 + 16);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+}
+
 template <int DT>
 __device__ __forceinline__ float smem_elem(const unsigned char* buf, int e) {
     return (DT == DT_BF16) ? __uint_as_float((uint32_t)(reinterpret_cast<const unsigned short*>(buf))[e] << 16)
@@ -92,7 +107,15 @@ __device__ __forceinline__ LSE smem_thread_lse(const unsigned char* buf, int n, 
     if (!(m > neg_inf()) || acc.bad) return acc;
     const float mc = m * c;
     float2 a0 = make_float2(0.f, 0.f), a1 = a0;
-    for (int e = (int)threadIdx.x * VEC; e < n; e += NT * VEC) {
+    int e = (int)threadIdx.x * VEC;
+    for (; e + NT * VEC + VEC <= n; e += 2 * NT * VEC) {  // two full vectors per iteration
+        float x[VEC], y[VEC];
+        smem_load8_full<DT>(buf, e, x);
+        smem_load8_full<DT>(buf, e + NT * VEC, y);
+        exp2_sum8(x, c, mc, a0, a1);
+        exp2_sum8(y, c, mc, a0, a1);
+    }
+    for (; e < n; e += NT * VEC) {  // at most one more vector, possibly ragged
         float x[VEC];
         smem_load8<DT>(buf, e, n, neg_inf(), x);
         exp2_sum8(x, c, mc, a0, a1);
@@ -129,53 +152,73 @@ __device__ __forceinline__ void smem_thread_lse2(const unsigned char* tb, const 
     d.s = (d0.x + d0.y) + (d1.x + d1.y);
 }
 
+// One 16-byte vector of a bf16 row in global memory at e (e a multiple of 8): elements
+// at or beyond hi read as -inf.
+__device__ __forceinline__ uint4 ld_bf16x8_ragged(const unsigned short* r, int e, int hi) {
+    if (e + VEC <= hi) return ld_nc_v4(r + e);
+    uint32_t w[4] = {0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u};
+    for (int j = 0; j < VEC && e + j < hi; ++j) {
+        const uint32_t h = (uint32_t)__ldg(r + e + j);
+        w[j >> 1] = (j & 1) ? ((w[j >> 1] & 0x0000ffffu) | (h << 16)) : ((w[j >> 1] & 0xffff0000u) | h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Maximum (NaN-propagating) of the eight bf16 values of a vector, as fp32.
+__device__ __forceinline__ float bf16x8_max(const uint4& v) {
+    const uint32_t pm = bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w));
+    return fmax_nan(bf16_lo(pm), bf16_hi(pm));
+}
+
+// Online (max, sum) update with a block of values whose maximum is vm: the running sum is
+// rescaled only when the maximum grows; a NaN maximum marks the partial invalid.
+__device__ __forceinline__ bool lse_online_max(LSE& acc, float& mc, float vm, float c, float2& a0, float2& a1) {
+    if (vm != vm) acc.bad = BAD_DATA;
+    if (vm > acc.m) {
+        const float f = ex2((acc.m - vm) * c);
+        a0 = fmul2(a0, make_float2(f, f));
+        a1 = fmul2(a1, make_float2(f, f));
+        acc.m = vm;
+        mc = vm * c;
+    }
+    return acc.m > neg_inf();
+}
+
+__device__ __forceinline__ void exp2_sum_bf16x8(const uint4& v, float c, float mc, float2& a0, float2& a1) {
+    const float x[VEC] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                          bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    exp2_sum8(x, c, mc, a0, a1);
+}
+
 // (max, sum 2^((l - max) c)) of one thread's share of elements [lo, hi) of a row in global
-// memory (16-byte aligned; lo a multiple of 8), online: four 16-byte vectors in flight per
-// thread, kept packed until used (bf16 rows: the maximum of a vector by max.bf16x2, no
-// unpacking), the running sum rescaled only when the maximum grows.
+// memory (16-byte aligned; lo a multiple of 8), online.  bf16 rows: groups of four 16-byte
+// vectors in flight per thread, kept packed until used; one maximum per group (max.bf16x2,
+// no unpacking) and one rescale test per group, then the exponentials; the vectors left
+// after the last full group one at a time.
 template <int DT>
 __device__ __forceinline__ LSE global_thread_lse(const void* row, int lo, int hi, float c) {
     if (DT != DT_BF16) return thread_lse<DT, 2>(row, lo, hi, true, c);
-    constexpr int U = 4;
+    constexpr int U = 4, STEP = NT * VEC;
     LSE acc{neg_inf(), 0.f, 0};
     float mc = 0.f;
     float2 a0 = make_float2(0.f, 0.f), a1 = a0;
     const unsigned short* r = reinterpret_cast<const unsigned short*>(row);
-    for (int e0 = lo + (int)threadIdx.x * VEC; e0 < hi; e0 += NT * VEC * U) {
+    int e0 = lo + (int)threadIdx.x * VEC;
+    for (; e0 + (U - 1) * STEP + VEC <= hi; e0 += U * STEP) {  // every vector of the group is full
         uint4 v[U];
-        bool full[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = e0 + u * NT * VEC;
-            full[u] = e + VEC <= hi;
-            v[u] = full[u] ? ld_nc_v4(r + e) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-            if (!full[u] && e < hi) {  // a ragged last vector: the elements before hi, -inf after
-                uint32_t w[4] = {0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u};
-                for (int j = 0; j < VEC && e + j < hi; ++j) {
-                    const uint32_t h = (uint32_t)__ldg(r + e + j);
-                    w[j >> 1] = (j & 1) ? ((w[j >> 1] & 0x0000ffffu) | (h << 16)) : ((w[j >> 1] & 0xffff0000u) | h);
-                }
-                v[u] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
+        for (int u = 0; u < U; ++u) v[u] = ld_nc_v4(r + e0 + u * STEP);
+        uint32_t pm = bmax2_nan(bmax2_nan(v[0].x, v[0].y), bmax2_nan(v[0].z, v[0].w));
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t pm = bmax2_nan(bmax2_nan(v[u].x, v[u].y), bmax2_nan(v[u].z, v[u].w));
-            const float vm = fmax_nan(bf16_lo(pm), bf16_hi(pm));
-            if (vm != vm) acc.bad = BAD_DATA;
-            if (vm > acc.m) {
-                const float f = ex2((acc.m - vm) * c);
-                a0 = fmul2(a0, make_float2(f, f));
-                a1 = fmul2(a1, make_float2(f, f));
-                acc.m = vm;
-                mc = vm * c;
-            }
-            if (acc.m > neg_inf()) {
-                const float x[VEC] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
-                                      bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
-                exp2_sum8(x, c, mc, a0, a1);
-            }
+        for (int u = 1; u < U; ++u) pm = bmax2_nan(pm, bmax2_nan(bmax2_nan(v[u].x, v[u].y), bmax2_nan(v[u].z, v[u].w)));
+        if (lse_online_max(acc, mc, fmax_nan(bf16_lo(pm), bf16_hi(pm)), c, a0, a1)) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) exp2_sum_bf16x8(v[u], c, mc, a0, a1);
         }
+    }
+    for (; e0 < hi; e0 += STEP) {  // fewer than U vectors left, the last possibly ragged
+        const uint4 v = ld_bf16x8_ragged(r, e0, hi);
+        if (lse_online_max(acc, mc, bf16x8_max(v), c, a0, a1)) exp2_sum_bf16x8(v, c, mc, a0, a1);
     }
     acc.s = (a0.x + a0.y) + (a1.x + a1.y);
     return acc;
@@ -327,34 +370,63 @@ struct StagedP {  // w = p = 2^((l - m) c) / S
         smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
         exp2_scale8(l, c, m * c, inv_s, w);
     }
+    __device__ __forceinline__ void eval8_full(int e0, float w[VEC]) const {
+        float l[VEC];
+        smem_load8_full<TDT>(tb, e0 - lo, l);
+        exp2_scale8(l, c, m * c, inv_s, w);
+    }
 };
 
 // w_j = max(0, p_j - q_j) from eight probabilities of each (exact subtraction, no contraction).
 __device__ __forceinline__ void residual8(const float p[VEC], const float q[VEC], float w[VEC]) {
 #pragma unroll
     for (int j = 0; j < VEC; j += 2) {
-        const float2 r = fadd2(make_float2(p[j], p[j + 1]), make_float2(-q[j], -q[j + 1]));
+        const float2 r = fsub2(make_float2(p[j], p[j + 1]), make_float2(q[j], q[j + 1]));
         w[j] = fmaxf(r.x, 0.f);
         w[j + 1] = fmaxf(r.y, 0.f);
     }
 }
 
-// w = max(0, p - q) with the target chunk staged and the draft-logit row read from
-// global memory (it was streamed for its statistics just before, so from L2).
+// Residual weights with the target chunk staged and the draft-logit row read from global
+// memory (it was streamed for its statistics just before, so from L2).  The draw needs
+// the weights only up to a common factor, so they are S_t * max(0, p - q) =
+// max(0, e_t - rho e_d), with e = 2^((l - M) c) and rho = S_t / S_d: one multiply per
+// element fewer than normalising both rows.  Where the two rows and their statistics are
+// equal, rho is exactly 1 and every weight exactly 0, as for p - q.
 template <int TDT, int DDT>
 struct StagedResidualD {
     static constexpr int kTilesInFlight = 4;  // global loads: several tiles in flight per warp
     const unsigned char* tb;
     const void* drow;
     int lo;
-    float c, mt, inv_st, md, inv_sd;
+    float c, mt, md, rho;
     __device__ __forceinline__ void eval8(int e0, int hi, float w[VEC]) const {
-        float l[VEC], d[VEC], p[VEC], q[VEC];
+        float l[VEC], d[VEC];
         smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
         load8<DDT>(drow, e0, hi, true, neg_inf(), d);
-        exp2_scale8(l, c, mt * c, inv_st, p);
-        exp2_scale8(d, c, md * c, inv_sd, q);
-        residual8(p, q, w);
+        weights(l, d, w);
+    }
+    __device__ __forceinline__ void eval8_full(int e0, float w[VEC]) const {
+        float l[VEC], d[VEC];
+        smem_load8_full<TDT>(tb, e0 - lo, l);
+        load8<DDT>(drow, e0, e0 + VEC, true, neg_inf(), d);
+        weights(l, d, w);
+    }
+    __device__ __forceinline__ void weights(float l[VEC], const float d[VEC], float w[VEC]) const {
+        float q[VEC];
+        const float2 cc = make_float2(c, c), mt2 = make_float2(-mt * c, -mt * c), md2 = make_float2(-md * c, -md * c);
+        const float2 rr = make_float2(rho, rho);
+#pragma unroll
+        for (int j = 0; j < VEC; j += 2) {
+            const float2 yt = ffma2(make_float2(l[j], l[j + 1]), cc, mt2);
+            const float2 yd = ffma2(make_float2(d[j], d[j + 1]), cc, md2);
+            const float2 qd = fmul2(make_float2(ex2(yd.x), ex2(yd.y)), rr);
+            l[j] = ex2(yt.x);
+            l[j + 1] = ex2(yt.y);
+            q[j] = qd.x;
+            q[j + 1] = qd.y;
+        }
+        residual8(l, q, w);
     }
 };
 
@@ -365,9 +437,19 @@ struct StagedResidual {  // w = max(0, p - q)
     int lo;
     float c, mt, inv_st, md, inv_sd;
     __device__ __forceinline__ void eval8(int e0, int hi, float w[VEC]) const {
-        float l[VEC], d[VEC], p[VEC];
+        float l[VEC], d[VEC];
         smem_load8<TDT>(tb, e0 - lo, hi - lo, neg_inf(), l);
         smem_load8<DDT>(db, e0 - lo, hi - lo, DK == DK_LOGITS ? neg_inf() : 0.f, d);
+        weights(l, d, w);
+    }
+    __device__ __forceinline__ void eval8_full(int e0, float w[VEC]) const {
+        float l[VEC], d[VEC];
+        smem_load8_full<TDT>(tb, e0 - lo, l);
+        smem_load8_full<DDT>(db, e0 - lo, d);
+        weights(l, d, w);
+    }
+    __device__ __forceinline__ void weights(const float l[VEC], const float d[VEC], float w[VEC]) const {
+        float p[VEC];
         exp2_scale8(l, c, mt * c, inv_st, p);
         if (DK == DK_LOGITS) {
             float q[VEC];

@@ -167,8 +167,9 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
                          (uint32_t)n * dsz, &bars[s]);
         }
     };
+    // thread 0 polls; every call is followed by a CTA barrier that releases the others
     auto wait_slot = [&](int s) -> bool {
-        const bool ok = mbar_wait_bounded(&bars[s], (par >> s) & 1u);
+        const bool ok = threadIdx.x != 0 || mbar_wait_bounded(&bars[s], (par >> s) & 1u);
         par ^= 1u << s;
         pend &= ~(1u << s);
         return ok;
@@ -256,8 +257,8 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
         // prefetch the children's rows into free slots (before the gathers below: the proxy
         // fence of a copy would otherwise wait for thread 0's outstanding loads).  A free
         // slot's reads ended at the barrier the walk passed when it descended; a dropped
-        // prefetch still in flight is waited for by every thread first.  Then one barrier
-        // and one proxy fence cover the whole batch of copies.
+        // prefetch still in flight is waited for first (by thread 0, which issues every
+        // copy).  Then one barrier and one proxy fence cover the whole batch of copies.
         {
             int sq[16], nq = 0;
             for (int q = 0; q < nchild && nq < 16; ++q) {
