@@ -965,19 +965,20 @@ __device__ DrawResult cluster_draw(const WF& wf, int lo, int hi, float u, float*
     const int nw = (int)(blockDim.x >> 5);  // warps of this CTA
     const int ntiles = (hi - lo + TILE - 1) / TILE;
     const int nfull = (hi - lo) / TILE;  // tiles with no element at or beyond hi
-    for (int t0 = warp * TB; t0 < ntiles; t0 += nw * TB) {
+    // each warp takes a contiguous run of tiles (runs differ by at most one tile), TB at a time
+    const int w_lo = (warp * ntiles) / nw, w_hi = ((warp + 1) * ntiles) / nw;
+    for (int t0 = w_lo; t0 < w_hi; t0 += TB) {
         float s[TB];  // each tile's weights are summed as soon as they are evaluated
-        const bool full = t0 + TB <= nfull;
 #pragma unroll
         for (int i = 0; i < TB; ++i) {
             s[i] = 0.f;
-            if (t0 + i < ntiles) {
+            if (t0 + i < w_hi) {
                 float w[VEC];
-                eval8_any(wf, lo + (t0 + i) * TILE + lane * VEC, hi, full, w);
+                eval8_any(wf, lo + (t0 + i) * TILE + lane * VEC, hi, t0 + i < nfull, w);
                 s[i] = sum8(w);
             }
         }
-        warp_tile_sums<TB>(s, lane, t0, ntiles, tile_sum);
+        warp_tile_sums<TB>(s, lane, t0, w_hi, tile_sum);
     }
     __syncthreads();
     return cluster_draw_from_tiles(wf, lo, hi, u, tile_sum, sc, phase, fail_in);

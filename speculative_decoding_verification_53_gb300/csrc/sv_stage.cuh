@@ -164,12 +164,6 @@ __device__ __forceinline__ uint4 ld_bf16x8_ragged(const unsigned short* r, int e
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Maximum (NaN-propagating) of the eight bf16 values of a vector, as fp32.
-__device__ __forceinline__ float bf16x8_max(const uint4& v) {
-    const uint32_t pm = bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w));
-    return fmax_nan(bf16_lo(pm), bf16_hi(pm));
-}
-
 // Online (max, sum) update with a block of values whose maximum is vm: the running sum is
 // rescaled only when the maximum grows; a NaN maximum marks the partial invalid.
 __device__ __forceinline__ bool lse_online_max(LSE& acc, float& mc, float vm, float c, float2& a0, float2& a1) {
@@ -191,34 +185,36 @@ __device__ __forceinline__ void exp2_sum_bf16x8(const uint4& v, float c, float m
 }
 
 // (max, sum 2^((l - max) c)) of one thread's share of elements [lo, hi) of a row in global
-// memory (16-byte aligned; lo a multiple of 8), online.  bf16 rows: groups of four 16-byte
-// vectors in flight per thread, kept packed until used; one maximum per group (max.bf16x2,
-// no unpacking) and one rescale test per group, then the exponentials; the vectors left
-// after the last full group one at a time.
+// memory (16-byte aligned; lo a multiple of 8), online.  bf16 rows: the thread's vectors in
+// groups of five, all five loads in flight at once and kept packed until used; one maximum
+// per group (max.bf16x2, no unpacking) and one rescale test per group, then the
+// exponentials.  Vectors at or beyond hi read as -inf and are skipped.  A CTA's share of a
+// 152064-element row split eight ways is 9 or 10 vectors per thread: two groups.
 template <int DT>
 __device__ __forceinline__ LSE global_thread_lse(const void* row, int lo, int hi, float c) {
     if (DT != DT_BF16) return thread_lse<DT, 2>(row, lo, hi, true, c);
-    constexpr int U = 4, STEP = NT * VEC;
+    constexpr int U = 5, STEP = NT * VEC;
     LSE acc{neg_inf(), 0.f, 0};
     float mc = 0.f;
     float2 a0 = make_float2(0.f, 0.f), a1 = a0;
     const unsigned short* r = reinterpret_cast<const unsigned short*>(row);
-    int e0 = lo + (int)threadIdx.x * VEC;
-    for (; e0 + (U - 1) * STEP + VEC <= hi; e0 += U * STEP) {  // every vector of the group is full
+    for (int e0 = lo + (int)threadIdx.x * VEC; e0 < hi; e0 += U * STEP) {
         uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = ld_nc_v4(r + e0 + u * STEP);
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * STEP;
+            v[u] = e + VEC <= hi ? ld_nc_v4(r + e)
+                                 : (e < hi ? ld_bf16x8_ragged(r, e, hi)
+                                           : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u));
+        }
         uint32_t pm = bmax2_nan(bmax2_nan(v[0].x, v[0].y), bmax2_nan(v[0].z, v[0].w));
 #pragma unroll
         for (int u = 1; u < U; ++u) pm = bmax2_nan(pm, bmax2_nan(bmax2_nan(v[u].x, v[u].y), bmax2_nan(v[u].z, v[u].w)));
         if (lse_online_max(acc, mc, fmax_nan(bf16_lo(pm), bf16_hi(pm)), c, a0, a1)) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) exp2_sum_bf16x8(v[u], c, mc, a0, a1);
+            for (int u = 0; u < U; ++u)
+                if (e0 + u * STEP < hi) exp2_sum_bf16x8(v[u], c, mc, a0, a1);
         }
-    }
-    for (; e0 < hi; e0 += STEP) {  // fewer than U vectors left, the last possibly ragged
-        const uint4 v = ld_bf16x8_ragged(r, e0, hi);
-        if (lse_online_max(acc, mc, bf16x8_max(v), c, a0, a1)) exp2_sum_bf16x8(v, c, mc, a0, a1);
     }
     acc.s = (a0.x + a0.y) + (a1.x + a1.y);
     return acc;
