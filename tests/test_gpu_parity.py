@@ -71,6 +71,21 @@ def test_staged_walk_one_slot(B, V):
     assert np.array_equal(g["tokens"][greedy], o["tokens"][greedy])
 
 
+@pytest.mark.parametrize("tdt,ddt", [("f32", "bf16"), ("bf16", "f32"), ("f32", "f32")])
+def test_staged_walk_one_slot_fp32_rows(tdt, ddt):
+    """The single-slot walk with fp32 target or draft-logit rows: the draft row is reduced
+    from global memory (fp32 loads) and re-read for the draw, the target staged."""
+    w = synth.mixed_batch(seed=61, B=160, K=3, V=16392)
+    if tdt == "f32":
+        w["target"] = synth.bf16_bits_to_f32(w["target"])
+    if ddt == "f32":
+        w["draft"] = synth.bf16_bits_to_f32(w["draft"])
+    g, o = gpu_chain(w, seed=5, offset=1), oracle_chain(w, seed=5, offset=1)
+    assert compare(g, o) <= 1
+    greedy = w["temperature"] <= 0
+    assert np.array_equal(g["tokens"][greedy], o["tokens"][greedy])
+
+
 def test_moderate_batch_position_parallel_with_bad_rows():
     """B = 32, V = 32000: the automatic path runs the position-parallel kernel in
     clusters of 2 over two waves.  Rows carry NaN, +inf, all -inf or an out-of-range
