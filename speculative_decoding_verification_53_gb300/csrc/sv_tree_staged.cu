@@ -38,7 +38,7 @@ __device__ __forceinline__ void hist_state(const TreeHist& hs, int n, int i, flo
     bool tried = false;
     for (int h = 1; h <= n; ++h) {
         const float qprev = tried ? 0.f : q0 * hs.qs[h - 1];
-        if (hs.applied[h - 1]) w = fmaxf(w * hs.zinv[h - 1] - qprev, 0.f);
+        if (hs.applied[h - 1]) w = fmaxf(fmaf(w, hs.zinv[h - 1], -qprev), 0.f);  // as the rejection pass
         tried |= (i == hs.x[h - 1]);
     }
     q = tried ? 0.f : q0 * hs.qs[n];
@@ -346,6 +346,11 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
                 // rejected: w_{h+1} = (w_h / Z_h - q_h)+ in place, with the residual mass and
                 // the mass of q without x
                 const float zi = h_zinv[nh], qsn = h_qs[nh];
+                // the arithmetic of hist_state, two lanes at a time: q0 = 2^(d c - md c) / S_d,
+                // w' = max(fma(w, 1/Z, -q0 qs), 0) (the negated q scale gives -q0 qs exactly)
+                const float2 cc = make_float2(c, c), zi2 = make_float2(zi, zi), nqs = make_float2(-qsn, -qsn);
+                const float2 md2 = make_float2(-node.mdc, -node.mdc), isd = make_float2(inv_sd, inv_sd);
+                const float2 mt2 = make_float2(-node.mtc, -node.mtc), ist = make_float2(inv_st, inv_st);
                 float2 part = make_float2(0.f, 0.f);
                 for (int e0 = lo + (int)threadIdx.x * VEC; e0 < hi; e0 += NT * VEC) {
                     const int o = e0 - lo;
@@ -357,18 +362,40 @@ __global__ void __launch_bounds__(NT, 2) tree_staged_kernel(const TreeArgs a, co
                         float l[VEC];
                         smem_load8<TDT>(tb, o, n, neg_inf(), l);
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) wv[j] = ex2(fmaf(l[j], c, -node.mtc)) * inv_st;
+                        for (int j = 0; j < VEC; j += 2) {
+                            const float2 y = ffma2(make_float2(l[j], l[j + 1]), cc, mt2);
+                            const float2 p = fmul2(make_float2(ex2(y.x), ex2(y.y)), ist);
+                            wv[j] = p.x;
+                            wv[j + 1] = p.y;
+                        }
                     }
-                    const uint32_t tw = tmask[o >> 5] >> (o & 31);  // 8 elements share a mask word
-                    float r[VEC];
+                    const uint32_t tw = (tmask[o >> 5] >> (o & 31)) & 0xffu;  // 8 elements share a mask word
+                    float r[VEC], nq[VEC];
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) {
-                        const float q0 = (DK == DK_LOGITS) ? ex2(fmaf(d[j], c, -node.mdc)) * inv_sd : d[j];
-                        const float qq = ((tw >> j) & 1u) ? 0.f : q0 * qsn;
-                        r[j] = fmaxf(wv[j] * zi - qq, 0.f);
-                        part.x += r[j];
-                        part.y += (e0 + j == x) ? 0.f : qq;
+                    for (int j = 0; j < VEC; j += 2) {
+                        float2 q0 = make_float2(d[j], d[j + 1]);
+                        if (DK == DK_LOGITS) {
+                            const float2 y = ffma2(q0, cc, md2);
+                            q0 = fmul2(make_float2(ex2(y.x), ex2(y.y)), isd);
+                        }
+                        const float2 nq2 = fmul2(q0, nqs);
+                        nq[j] = nq2.x;
+                        nq[j + 1] = nq2.y;
                     }
+                    if (tw) {  // tried tokens in this vector weigh nothing in q
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j)
+                            if ((tw >> j) & 1u) nq[j] = 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < VEC; j += 2) {
+                        const float2 rr = ffma2(make_float2(wv[j], wv[j + 1]), zi2, make_float2(nq[j], nq[j + 1]));
+                        r[j] = fmaxf(rr.x, 0.f);
+                        r[j + 1] = fmaxf(rr.y, 0.f);
+                    }
+                    part.x += sum8(r);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) part.y -= (e0 + j == x) ? 0.f : nq[j];
                     if (o + VEC <= n) {
                         *reinterpret_cast<float4*>(wbuf + o) = make_float4(r[0], r[1], r[2], r[3]);
                         *reinterpret_cast<float4*>(wbuf + o + 4) = make_float4(r[4], r[5], r[6], r[7]);
