@@ -598,6 +598,73 @@ def _packed(arrays, device, copies=1):
     return host, devs, views
 
 
+def _run_e2e_chain_host(w, device, stream, rows, n, kind):
+    """The chain's round trip through spec_verify_chain_host (the C entry that takes host
+    buffers): every step one copy of the packed inputs in, the verify, one copy of the
+    tokens and counts out.  Two streams alternate, each with its own device buffers and
+    workspace, so a step's copy in overlaps the previous step's verify, as a serving loop
+    would pipeline them.  The entry is called through ctypes with its arguments prepared
+    once, so the host does not pace the loop."""
+    import ctypes
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    sl = slice(0, rows)
+    K, V = w["tokens"].shape[1], w["target"].shape[2]
+    tdt = torch.bfloat16 if w["target"].dtype == np.uint16 else torch.float32
+    ddt = torch.bfloat16 if w["draft"].dtype == np.uint16 else torch.float32
+    offs, nin, nout = sv.spec_verify_host_sizes(rows, K, V, target_dtype=tdt, draft_dtype=ddt, draft_kind=kind)
+    hin = torch.zeros(nin, dtype=torch.uint8).pin_memory()
+    hv = hin.numpy()
+    for o, k in zip(offs, ("target", "draft", "tokens", "temperature")):
+        a = np.ascontiguousarray(w[k][sl])
+        hv[o:o + a.nbytes] = np.frombuffer(a.tobytes(), dtype=np.uint8)
+    streams = [stream, torch.cuda.Stream(device)]
+    dins = [torch.empty(nin, dtype=torch.uint8, device=device) for _ in range(2)]
+    douts = [torch.empty(nout, dtype=torch.uint8, device=device) for _ in range(2)]
+    houts = [torch.zeros(nout, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    ws_bytes = max(sv.spec_verify_workspace_size(rows, K, V), 256)
+    wss = [torch.zeros(ws_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    fn = sv.lib().spec_verify_chain_host
+    vp = ctypes.c_void_p
+    codes = (sv.SV_BF16 if tdt == torch.bfloat16 else sv.SV_F32, sv.SV_BF16 if ddt == torch.bfloat16 else sv.SV_F32,
+             sv.SV_DRAFT_PROBS if kind == "probs" else sv.SV_DRAFT_LOGITS)
+    per = [(vp(hin.data_ptr()), vp(dins[j].data_ptr()), vp(houts[j].data_ptr()), vp(douts[j].data_ptr()))
+           + codes + (rows, K, V) for j in range(2)]
+    tail = [(vp(wss[j].data_ptr()), ws_bytes, vp(streams[j].cuda_stream)) for j in range(2)]
+
+    def one(i):
+        j = i & 1
+        st = fn(*per[j], 23, i, *tail[j])
+        if st != sv.SV_OK:
+            raise sv.SpecVerifyError(st, "spec_verify_chain_host")
+
+    for i in range(4):
+        one(i)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    other = torch.cuda.Event()
+    start.record(streams[0])
+    streams[1].wait_event(start)
+    for i in range(n):
+        one(i)
+    other.record(streams[1])
+    streams[0].wait_event(other)
+    end.record(streams[0])
+    torch.cuda.synchronize(device)
+    ms = start.elapsed_time(end)
+    for j in range(2):  # the device copy holds the inputs, and every row of the last steps verified
+        if not torch.equal(dins[j].cpu(), hin):
+            raise RuntimeError("end-to-end staging of the inputs is wrong")
+        counts = houts[j].view(torch.int32)[rows * (K + 1):]
+        if not (counts >= 1).all():
+            raise RuntimeError("end-to-end counts are not all valid")
+    return {"value": rows * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(nin),
+            "d2h_bytes_per_step": int(nout), "steps": n, "ms_per_step": ms / n,
+            "staging": "spec_verify_chain_host: inputs packed in one pinned buffer (one copy in), tokens and counts "
+                       "in one (one copy out); two streams alternate, so a step's copy in overlaps the previous "
+                       "step's verify"}
+
+
 def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
     """Through the public API with host buffers, every step: the step's inputs copied from
     pinned host memory (staged back to back, one copy), the verify call (outputs and
@@ -617,6 +684,8 @@ def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
     else:
         names = ["target", "draft", "tokens", "temperature"]
         out_cols = w["tokens"].shape[1] + 1
+    if not tree and not w.get("sample"):
+        return _run_e2e_chain_host(w, device, stream, per_step_rows, n, kind)
     hin, dins, vs = _packed([w[k][sl] for k in names], device)
     din, views = dins[0], vs[0]
     # outputs back to back in one device buffer: tokens [B][cols], count [B] (and the

@@ -157,6 +157,39 @@ SV_API sv_status spec_verify_chain_noalloc(const void *target_logits, sv_dtype t
                                     void *stream);
 
 /*
+ * Chain verify from host memory (the pages have no counterpart: this is the serving
+ * loop's round trip).  One call enqueues on `stream`, without synchronising:
+ *   1. one host-to-device copy of a round's packed inputs, h_in -> d_in;
+ *   2. spec_verify_chain on views of d_in, writing into d_out;
+ *   3. one device-to-host copy of the outputs, d_out -> h_out.
+ * The packed input layout, each part starting at a multiple of 256 bytes:
+ *   target [B][K+1][V] (tdt), draft [B][K][V] (ddt, fp32 for SV_DRAFT_PROBS),
+ *   tokens int32 [B][K], temperature fp32 [B].
+ * The packed output layout: tokens int32 [B][K+1], then counts int32 [B].
+ *   h_in, h_out    host buffers; page-locked (pinned) for the copies to be asynchronous.
+ *   d_in, d_out    device buffers of in_bytes and out_bytes (spec_verify_host_sizes).
+ *   workspace, ws_bytes  as spec_verify_chain.
+ * The outputs in h_out are valid once the stream has reached this call's end (an event
+ * or a synchronisation).  Alternating two d_in / d_out pairs over two streams overlaps
+ * one round's copy with the previous round's verify.  Errors: those of
+ * spec_verify_chain; SV_ERR_INVALID_ARG for a NULL buffer; SV_ERR_CUDA when a copy cannot
+ * be enqueued.
+ */
+SV_API sv_status spec_verify_chain_host(const void *h_in, void *d_in, void *h_out, void *d_out,
+                                        sv_dtype tdt, sv_dtype ddt, sv_draft_kind dk, int B, int K, int V,
+                                        uint64_t seed, uint64_t offset, void *workspace, size_t ws_bytes,
+                                        void *stream);
+
+/*
+ * Sizes of spec_verify_chain_host's packed buffers.  offsets (nullable) receives 4
+ * byte offsets into the packed input: target, draft, tokens, temperature.  Returns
+ * SV_ERR_INVALID_ARG for sizes outside spec_verify_chain's limits or an unknown dtype
+ * or kind.
+ */
+SV_API sv_status spec_verify_host_sizes(int B, int K, int V, sv_dtype tdt, sv_dtype ddt, sv_draft_kind dk,
+                                        size_t *offsets, size_t *in_bytes, size_t *out_bytes);
+
+/*
  * Greedy acceptance (the temperature-0 rule) for every row:
  *   target_logits device [B][K+1][V] (tdt), draft_tokens device int32 [B][K];
  *   out_tokens device int32 [B][K+1], out_count device int32 [B].

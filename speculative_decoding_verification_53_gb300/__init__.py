@@ -26,7 +26,8 @@ SV_SIBLINGS_WITHOUT_REPLACEMENT, SV_SIBLINGS_IID = 0, 1
 EXPORTS = ("spec_verify_workspace_size", "spec_verify_chain", "spec_greedy_accept", "spec_verify_tree",
            "spec_verify_status_string", "spec_verify_last_cuda_error", "spec_verify_chain_noalloc",
            "spec_tree_mask", "spec_kv_compact", "spec_verify_tree_rule", "spec_sample_and_verify",
-           "spec_verify_count_invalid", "spec_verify_rows_status")
+           "spec_verify_count_invalid", "spec_verify_rows_status", "spec_verify_chain_host",
+           "spec_verify_host_sizes")
 
 # out_count value of a batch row whose kernel gave up a bounded device-side wait
 COUNT_TIMEOUT = -1
@@ -81,6 +82,10 @@ def lib() -> ctypes.CDLL:
     L.spec_verify_count_invalid.restype = ci
     L.spec_verify_rows_status.argtypes = [vp, ci, vp, vp]
     L.spec_verify_rows_status.restype = ci
+    L.spec_verify_chain_host.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, u64, u64, vp, sz, vp]
+    L.spec_verify_chain_host.restype = ci
+    L.spec_verify_host_sizes.argtypes = [ci, ci, ci, ci, ci, ci, vp, vp, vp]
+    L.spec_verify_host_sizes.restype = ci
     _lib = L
     return L
 
@@ -119,6 +124,16 @@ def _dev(t, name, dtype=None):
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     return t
+
+
+def _dtype_code_of(dtype) -> int:
+    """The sv_dtype of a torch dtype (float32 or bfloat16)."""
+    torch = _torch()
+    if dtype == torch.float32:
+        return SV_F32
+    if dtype == torch.bfloat16:
+        return SV_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {dtype}")
 
 
 def _ptr(t):
@@ -333,6 +348,33 @@ def spec_verify_count_invalid(out_count, *, out_invalid=None, stream=None):
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_count_invalid")
     return out_invalid
+
+
+def spec_verify_host_sizes(B: int, K: int, V: int, *, target_dtype, draft_dtype, draft_kind):
+    """(offsets of target, draft, tokens, temperature in the packed input, input bytes,
+    output bytes) of spec_verify_chain_host's buffers; dtypes are torch dtypes."""
+    off = (ctypes.c_size_t * 4)()
+    nin, nout = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = lib().spec_verify_host_sizes(B, K, V, _dtype_code_of(target_dtype), _dtype_code_of(draft_dtype),
+                                      _kind(draft_kind), ctypes.cast(off, ctypes.c_void_p), ctypes.byref(nin),
+                                      ctypes.byref(nout))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_host_sizes")
+    return tuple(off), nin.value, nout.value
+
+
+def spec_verify_chain_host(h_in, d_in, h_out, d_out, B: int, K: int, V: int, seed: int, offset: int, *,
+                           target_dtype, draft_dtype, draft_kind, workspace=None, stream=None):
+    """One round from host memory: h_in (pinned uint8, the packed inputs of
+    spec_verify_host_sizes) copied into d_in (uint8 CUDA), the chain verify, and the
+    tokens [B][K+1] then counts [B] (int32) copied from d_out into h_out (pinned), all
+    enqueued on the stream.  h_out holds them once the stream has passed this call."""
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    st = lib().spec_verify_chain_host(h_in.data_ptr(), _ptr(d_in), h_out.data_ptr(), _ptr(d_out),
+                                      _dtype_code_of(target_dtype), _dtype_code_of(draft_dtype), _kind(draft_kind),
+                                      B, K, V, int(seed), int(offset), ws_ptr, ws_bytes, _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_chain_host")
 
 
 def spec_verify_rows_status(out_count, *, out_status=None, stream=None):

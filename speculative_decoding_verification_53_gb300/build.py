@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspecverify.so")
 SOURCES = ["sv_api.cu", "sv_chain.cu", "sv_chain_staged.cu", "sv_chain_spec.cu", "sv_chain_eager.cu", "sv_chain_ring.cu",
-           "sv_tree.cu", "sv_tree_staged.cu", "sv_noalloc.cu", "sv_tree_kv.cu", "sv_sample.cu", "sv_status.cu",
+           "sv_tree.cu", "sv_tree_staged.cu", "sv_noalloc.cu", "sv_host.cu", "sv_tree_kv.cu", "sv_sample.cu", "sv_status.cu",
            "sv_launch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
