@@ -110,6 +110,37 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     assert c(None, 4, vp, None) == sv.SV_ERR_INVALID_ARG
 
 
+def test_host_round_trip_sizes_and_argument_errors(lib):
+    """spec_verify_host_sizes: the packed input's parts start on 256-byte boundaries in the
+    documented order and cover their arrays; the output is tokens then counts.  The host
+    entry rejects bad sizes and NULL buffers before anything is enqueued."""
+    import speculative_decoding_verification_53_gb300 as sv
+    off = (ctypes.c_size_t * 4)()
+    nin, nout = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    B, K, V = 3, 5, 1001
+    st = lib.spec_verify_host_sizes(B, K, V, sv.SV_BF16, sv.SV_F32, sv.SV_DRAFT_PROBS, ctypes.cast(off, ctypes.c_void_p),
+                                    ctypes.byref(nin), ctypes.byref(nout))
+    assert st == sv.SV_OK
+    parts = [B * (K + 1) * V * 2, B * K * V * 4, B * K * 4, B * 4]  # target, draft, tokens, temperature
+    assert off[0] == 0 and all(o % 256 == 0 for o in off) and nin.value % 256 == 0
+    for i in range(3):
+        assert off[i] + parts[i] <= off[i + 1] < off[i] + parts[i] + 256
+    assert off[3] + parts[3] <= nin.value < off[3] + parts[3] + 256
+    assert nout.value == B * (K + 2) * 4
+    hs = lib.spec_verify_host_sizes
+    nul = None
+    assert hs(1, 65, 100, 0, 0, 0, nul, nul, nul) == sv.SV_ERR_INVALID_ARG           # K over 64
+    assert hs(1, 4, 100, 1, 1, 0, nul, nul, nul) == sv.SV_ERR_INVALID_ARG            # bf16 probabilities
+    assert hs(1, 4, 100, 2, 0, 0, nul, nul, nul) == sv.SV_ERR_INVALID_ARG            # unknown dtype
+    assert hs(0, 4, 100, 0, 0, 0, nul, nul, nul) == sv.SV_OK
+    h = lib.spec_verify_chain_host
+    vp = ctypes.c_void_p(16)  # never dereferenced: the checks come first
+    assert h(vp, vp, vp, vp, 0, 0, 0, -1, 4, 100, 0, 0, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert h(vp, None, vp, vp, 0, 0, 0, 1, 4, 100, 0, 0, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert h(vp, vp, vp, None, 0, 0, 0, 1, 4, 100, 0, 0, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert h(None, None, None, None, 0, 0, 0, 0, 4, 100, 0, 0, None, 0, None) == sv.SV_OK  # empty batch
+
+
 def test_binding_refuses_to_run_without_the_library(monkeypatch, tmp_path):
     import speculative_decoding_verification_53_gb300 as sv
     monkeypatch.setattr(sv, "LIB_PATH", str(tmp_path / "missing.so"))
