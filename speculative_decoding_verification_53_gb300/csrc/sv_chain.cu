@@ -185,12 +185,9 @@ static cudaError_t launch_chain_t(const ChainArgs& a, int G, cudaStream_t stream
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.stream = stream;
-    cfg.dynamicSmemBytes = draw_smem_bytes(a.V, 1);
-    int max_cluster = 0;  // largest cluster the device co-schedules for this kernel
-    const cudaError_t e = cache.max_cluster((const void*)kern, cfg, &max_cluster);
+    const cudaError_t e = cache.pick_cluster((const void*)kern, cfg, G, [&](int g) { return draw_smem_bytes(a.V, g); }, &G);
     if (e != cudaSuccess) return e;
-    if (max_cluster < 1) max_cluster = 1;
-    while (G > max_cluster) G >>= 1;
+    if (G == 0) return cudaErrorInvalidValue;  // no cluster size fits the draw's tile sums
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.B, 1);
     cfg.dynamicSmemBytes = draw_smem_bytes(a.V, G);
     cudaLaunchAttribute attr[2];

@@ -155,6 +155,28 @@ public:
     cudaError_t max_cluster(const void* kern, const cudaLaunchConfig_t& cfg, int* out);
     // Clusters of G CTAs resident at once for that launch shape (cudaOccupancyMaxActiveClusters).
     cudaError_t active_clusters(const void* kern, const cudaLaunchConfig_t& cfg, int G, int* out);
+    // The cluster size to launch a kernel whose dynamic shared memory depends on it
+    // (smem_for(G)): the requested size when the device co-schedules it with that memory,
+    // else the nearest smaller size that it does, else the nearest larger one (a larger
+    // cluster gives each CTA a smaller chunk).  *G is 0 when no size up to 16 fits.
+    template <class SmemFor>
+    cudaError_t pick_cluster(const void* kern, cudaLaunchConfig_t cfg, int want, SmemFor smem_for, int* G) {
+        *G = 0;
+        int cand[10], nc = 0;
+        for (int g = want; g >= 1; g >>= 1) cand[nc++] = g;
+        for (int g = want * 2; g <= 16; g <<= 1) cand[nc++] = g;
+        for (int i = 0; i < nc; ++i) {
+            cfg.dynamicSmemBytes = smem_for(cand[i]);
+            int maxc = 0;
+            const cudaError_t e = max_cluster(kern, cfg, &maxc);
+            if (e != cudaSuccess) return e;
+            if (maxc >= cand[i]) {
+                *G = cand[i];
+                return cudaSuccess;
+            }
+        }
+        return cudaSuccess;
+    }
 
 private:
     static constexpr int kDevices = 64;

@@ -172,12 +172,17 @@ static cudaError_t sample_cluster(long long BK, int V, int& G_out) {
 template <int DDT>
 static cudaError_t launch_sample_t(const SampleArgs& a, cudaStream_t stream) {
     auto kern = draft_sample_kernel<DDT>;
+    static KernelLaunchCache cache;
     int G = 1;
     cudaError_t e = sample_cluster<DDT>((long long)a.B * a.K, a.V, G);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.stream = stream;
+    // a cluster size whose draw tile sums fit in shared memory (very large rows need G > 1)
+    e = cache.pick_cluster((const void*)kern, cfg, G, [&](int g) { return draw_smem_bytes(a.V, g); }, &G);
+    if (e != cudaSuccess) return e;
+    if (G == 0) return cudaErrorInvalidValue;
     cfg.gridDim = dim3((unsigned)G, (unsigned)a.K, (unsigned)a.B);
     cfg.dynamicSmemBytes = draw_smem_bytes(a.V, G);
     cudaLaunchAttribute attr[2];

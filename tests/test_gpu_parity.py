@@ -5,6 +5,8 @@ draft probabilities, mixed greedy/sampling batch, draft trees, large batch
 V=152064 at three temperatures), ragged and misaligned vocabularies, and the
 degenerate cases (K=0, V=1, ties, masked and invalid rows).
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -187,6 +189,29 @@ def test_tree_small_random_shapes():
     assert compare(gpu_tree(wp), oracle_tree(wp), keys=("tokens", "count", "path")) <= 1
 
 
+def test_tree_at_the_node_and_depth_limits():
+    """N = 1024 nodes (16 chains of 64 under the root, so depth 64 = max_depth): the walk
+    may descend 64 levels; greedy and sampling against the oracle, draft as logits."""
+    rng = np.random.default_rng(5)
+    B, N, V, D = 2, 1024, 2048, 64
+    target = rng.normal(0, 2, (B, N + 1, V)).astype(np.float32)
+    draft = (target + rng.normal(0, 0.3, (B, N + 1, V))).astype(np.float32)
+    par = np.array([i - 16 if i >= 16 else -1 for i in range(N)], np.int32)
+    par = np.tile(par, (B, 1))
+    toks = rng.integers(0, V, (B, N)).astype(np.int32)
+    for b in range(B):  # most nodes carry the target's argmax of their parent's row: long accepted paths
+        for i in range(N):
+            if rng.random() < 0.97:
+                toks[b, i] = int(np.argmax(target[b, par[b, i] + 1]))
+    for T in (0.0, 1.0):
+        w = dict(kind="tree", target=target, draft=draft, draft_kind=oracle.DRAFT_LOGITS, node_tokens=toks,
+                 parent=par, temperature=np.full(B, T, np.float32), max_depth=D, seed=2, offset=0)
+        g, o = gpu_tree(w), oracle_tree(w)
+        assert compare(g, o, keys=("tokens", "count", "path")) <= 1
+        if T == 0.0:
+            assert o["count"].min() > 8  # greedy walks go deep
+
+
 # ------------------------------------------------------------ edge cases
 
 @pytest.mark.parametrize("V", [1, 7, 9, 255, 1001, 4097, 33001])
@@ -200,6 +225,27 @@ def test_ragged_and_misaligned_vocab(V, dt):
     wg = dict(w)
     wg["temperature"] = np.zeros(37, np.float32)
     assert compare(gpu_chain(wg), oracle_chain(wg)) == 0
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_largest_vocabulary(dt):
+    """V = 2^24, the largest vocabulary the boundary takes: a chunk per CTA far beyond shared
+    memory, so the rows are streamed; greedy and sampling rows against the oracle.  One more
+    element is refused before anything runs."""
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    V = 1 << 24
+    w = synth.tiny_chain(seed=91, V=V, K=1, B=2, temperature=1.0)
+    w["temperature"] = np.array([1.0, 0.0], np.float32)  # a sampling row and a greedy row
+    if dt == "bf16":
+        w["target"] = synth.f32_to_bf16_bits(w["target"])
+        w["draft"] = synth.f32_to_bf16_bits(w["draft"])
+    assert compare(gpu_chain(w, seed=4, offset=1), oracle_chain(w, seed=4, offset=1)) <= 1
+    t = torch.zeros((1, 2, 8), dtype=torch.float32, device="cuda")
+    st = sv.lib().spec_verify_chain(ctypes.c_void_p(t.data_ptr()), 0, ctypes.c_void_p(t.data_ptr()), 0, 1,
+                                    ctypes.c_void_p(t.data_ptr()), ctypes.c_void_p(t.data_ptr()), 1, 1, V + 1, 0, 0,
+                                    ctypes.c_void_p(t.data_ptr()), ctypes.c_void_p(t.data_ptr()), None, None, 0, None)
+    assert st == sv.SV_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("K", [0, 1, 2, 64])
