@@ -47,6 +47,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verify rows/s and achieved HBM GB/s vs GB300 peak at V=128256, K=5"
 UNIT = "verify rows/s"
+# streams that take the end-to-end chain steps in turn (a copy's fixed start-up latency overlaps
+# the steps before it; past four the host-to-device link is the bound)
+E2E_STREAMS = 4
 FALLBACK_HBM_GBS = 6800.0
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -601,10 +604,11 @@ def _packed(arrays, device, copies=1):
 def _run_e2e_chain_host(w, device, stream, rows, n, kind):
     """The chain's round trip through spec_verify_chain_host (the C entry that takes host
     buffers): every step one copy of the packed inputs in, the verify, one copy of the
-    tokens and counts out.  Two streams alternate, each with its own device buffers and
-    workspace, so a step's copy in overlaps the previous step's verify, as a serving loop
-    would pipeline them.  The entry is called through ctypes with its arguments prepared
-    once, so the host does not pace the loop."""
+    tokens and counts out.  E2E_STREAMS streams take the steps in turn, each with its own
+    device buffers and workspace, so a step's copy in overlaps the verifies (and the fixed
+    start-up latency of the copies) of the steps before it, as a serving loop with several
+    independent requests in flight would pipeline them.  The entry is called through ctypes
+    with its arguments prepared once, so the host does not pace the loop."""
     import ctypes
     import torch
     import speculative_decoding_verification_53_gb300 as sv
@@ -618,41 +622,44 @@ def _run_e2e_chain_host(w, device, stream, rows, n, kind):
     for o, k in zip(offs, ("target", "draft", "tokens", "temperature")):
         a = np.ascontiguousarray(w[k][sl])
         hv[o:o + a.nbytes] = np.frombuffer(a.tobytes(), dtype=np.uint8)
-    streams = [stream, torch.cuda.Stream(device)]
-    dins = [torch.empty(nin, dtype=torch.uint8, device=device) for _ in range(2)]
-    douts = [torch.empty(nout, dtype=torch.uint8, device=device) for _ in range(2)]
-    houts = [torch.zeros(nout, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    ns = E2E_STREAMS
+    streams = [stream] + [torch.cuda.Stream(device) for _ in range(ns - 1)]
+    dins = [torch.empty(nin, dtype=torch.uint8, device=device) for _ in range(ns)]
+    douts = [torch.empty(nout, dtype=torch.uint8, device=device) for _ in range(ns)]
+    houts = [torch.zeros(nout, dtype=torch.uint8).pin_memory() for _ in range(ns)]
     ws_bytes = max(sv.spec_verify_workspace_size(rows, K, V), 256)
-    wss = [torch.zeros(ws_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    wss = [torch.zeros(ws_bytes, dtype=torch.uint8, device=device) for _ in range(ns)]
     fn = sv.lib().spec_verify_chain_host
     vp = ctypes.c_void_p
     codes = (sv.SV_BF16 if tdt == torch.bfloat16 else sv.SV_F32, sv.SV_BF16 if ddt == torch.bfloat16 else sv.SV_F32,
              sv.SV_DRAFT_PROBS if kind == "probs" else sv.SV_DRAFT_LOGITS)
     per = [(vp(hin.data_ptr()), vp(dins[j].data_ptr()), vp(houts[j].data_ptr()), vp(douts[j].data_ptr()))
-           + codes + (rows, K, V) for j in range(2)]
-    tail = [(vp(wss[j].data_ptr()), ws_bytes, vp(streams[j].cuda_stream)) for j in range(2)]
+           + codes + (rows, K, V) for j in range(ns)]
+    tail = [(vp(wss[j].data_ptr()), ws_bytes, vp(streams[j].cuda_stream)) for j in range(ns)]
 
     def one(i):
-        j = i & 1
+        j = i % ns
         st = fn(*per[j], 23, i, *tail[j])
         if st != sv.SV_OK:
             raise sv.SpecVerifyError(st, "spec_verify_chain_host")
 
-    for i in range(4):
+    for i in range(2 * ns):
         one(i)
     torch.cuda.synchronize(device)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    other = torch.cuda.Event()
     start.record(streams[0])
-    streams[1].wait_event(start)
+    for s in streams[1:]:
+        s.wait_event(start)
     for i in range(n):
         one(i)
-    other.record(streams[1])
-    streams[0].wait_event(other)
+    for s in streams[1:]:
+        done = torch.cuda.Event()
+        done.record(s)
+        streams[0].wait_event(done)
     end.record(streams[0])
     torch.cuda.synchronize(device)
     ms = start.elapsed_time(end)
-    for j in range(2):  # the device copy holds the inputs, and every row of the last steps verified
+    for j in range(ns):  # the device copy holds the inputs, and every row of the last steps verified
         if not torch.equal(dins[j].cpu(), hin):
             raise RuntimeError("end-to-end staging of the inputs is wrong")
         counts = houts[j].view(torch.int32)[rows * (K + 1):]
@@ -661,8 +668,8 @@ def _run_e2e_chain_host(w, device, stream, rows, n, kind):
     return {"value": rows * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(nin),
             "d2h_bytes_per_step": int(nout), "steps": n, "ms_per_step": ms / n,
             "staging": "spec_verify_chain_host: inputs packed in one pinned buffer (one copy in), tokens and counts "
-                       "in one (one copy out); two streams alternate, so a step's copy in overlaps the previous "
-                       "step's verify"}
+                       f"in one (one copy out); {ns} streams take the steps in turn, so a step's copy in overlaps "
+                       "the verifies of the steps before it"}
 
 
 def run_e2e(args, w, device, stream, tree, per_step_rows, n_inputs, kind):
