@@ -248,6 +248,32 @@ def test_largest_vocabulary(dt):
     assert st == sv.SV_ERR_INVALID_ARG
 
 
+def test_largest_batch():
+    """B = 65535, the most batch rows the boundary takes: a chain with greedy and sampling
+    rows, and a two-level tree per row, against the oracle at a small vocabulary; one row
+    more is refused before anything runs."""
+    import torch
+    import speculative_decoding_verification_53_gb300 as sv
+    B = 65535
+    w = synth.tiny_chain(seed=77, V=64, K=2, B=B, temperature=0.9)
+    w["temperature"][::3] = 0.0
+    assert compare(gpu_chain(w, seed=9, offset=2), oracle_chain(w, seed=9, offset=2)) <= B // 2000
+    rng = np.random.default_rng(8)
+    N, V = 3, 32
+    target = rng.normal(0, 2, (B, N + 1, V)).astype(np.float32)
+    draft = (target + rng.normal(0, 1, (B, N + 1, V))).astype(np.float32)
+    par = np.tile(np.array([-1, 0, -1], np.int32), (B, 1))  # root -> {0 -> 1, 2}
+    toks = rng.integers(0, V, (B, N)).astype(np.int32)
+    temp = np.where(np.arange(B) % 4 == 0, 0.0, 1.0).astype(np.float32)
+    wt = dict(kind="tree", target=target, draft=draft, draft_kind=oracle.DRAFT_LOGITS, node_tokens=toks,
+              parent=par, temperature=temp, max_depth=2, seed=6, offset=0)
+    assert compare(gpu_tree(wt), oracle_tree(wt), keys=("tokens", "count", "path")) <= B // 2000
+    t = torch.zeros((1, 2, 8), dtype=torch.float32, device="cuda")
+    p = ctypes.c_void_p(t.data_ptr())
+    st = sv.lib().spec_verify_chain(p, 0, p, 0, 1, p, p, B + 1, 1, 8, 0, 0, p, p, None, None, 0, None)
+    assert st == sv.SV_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("K", [0, 1, 2, 64])
 def test_draft_length_extremes(K):
     w = synth.tiny_chain(seed=K, V=513, K=K, B=20, temperature=1.0, sigma=0.2)
