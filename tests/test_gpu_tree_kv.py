@@ -180,3 +180,44 @@ def test_kv_compact_bad_arguments(sv):
     assert f(arr, 1, 0, 0, 1, 16, 16, 8, vp, vp, None, 1, 65, None) == sv.SV_ERR_INVALID_ARG  # depth 65
     assert f(arr, 1, 0, 0, 1, 16, 16, 8, None, vp, None, 1, 4, None) == sv.SV_ERR_INVALID_ARG  # no path
     assert f(arr, 1, 0, 0, 1, 16, 16, 8, None, None, None, 0, 4, None) == sv.SV_OK            # empty batch
+
+
+@pytest.mark.parametrize("N", [12, 70])
+def test_mask_at_the_largest_batch(sv, N):
+    """B = 65535 trees, the most the boundary takes, through the small-tree kernel (N <= 64)
+    and the general one; one tree more is refused before anything runs."""
+    import ctypes
+    B = 65535
+    par = synth.random_parents(23 + N, B, N, max_depth=8)
+    m, d, v = _gpu_mask(sv, par)
+    o = oracle.tree_mask(par)
+    assert (v == o["valid"]).all() and (m == o["mask"]).all() and (d == o["depth"]).all()
+    vp = ctypes.c_void_p(16)  # never dereferenced: the size check comes first
+    assert sv.lib().spec_tree_mask(vp, B + 1, N, vp, None, None, None) == sv.SV_ERR_INVALID_ARG
+
+
+def test_kv_compact_at_its_limits(sv):
+    """256 cache tensors in one call (the most it takes) and B = 65535 batch rows, every
+    byte against the oracle; 257 tensors or one row more are refused before anything runs."""
+    import ctypes
+    import torch
+    B, N, D, H, R, width = 3, 20, 5, 2, 24, 16
+    kv, path, count, base = _kv_case(51, B, N, D, H, R, width, 256)
+    dev = [torch.from_numpy(k).cuda() for k in kv]
+    sv.spec_kv_compact(dev, torch.from_numpy(path).cuda(), torch.from_numpy(count).cuda(),
+                       torch.from_numpy(base).cuda())
+    torch.cuda.synchronize()
+    for t, w in zip(dev, _oracle_kv(list(kv), path, count, base)):
+        assert (t.cpu().numpy() == w).all()
+    B, N, D, H, R, width = 65535, 12, 4, 1, 16, 4
+    kv, path, count, base = _kv_case(52, B, N, D, H, R, width, 1)
+    dev = [torch.from_numpy(k).cuda() for k in kv]
+    sv.spec_kv_compact(dev, torch.from_numpy(path).cuda(), torch.from_numpy(count).cuda(),
+                       torch.from_numpy(base).cuda())
+    torch.cuda.synchronize()
+    assert (dev[0].cpu().numpy() == _oracle_kv(list(kv), path, count, base)[0]).all()
+    vp = ctypes.c_void_p(16)  # never dereferenced: the size checks come first
+    arr = (ctypes.c_void_p * 257)(*([16] * 257))
+    f = sv.lib().spec_kv_compact
+    assert f(arr, 257, 0, 0, 1, 16, 16, 8, vp, vp, None, 1, 4, None) == sv.SV_ERR_INVALID_ARG
+    assert f(arr, 1, 0, 0, 1, 16, 16, 8, vp, vp, None, 65536, 4, None) == sv.SV_ERR_INVALID_ARG
