@@ -101,3 +101,28 @@ def test_sample_and_verify_bad_arguments(sv):
     assert f(vp, 0, None, 0, vp, 1, 3, 100, 0, 0, vp, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
     assert f(vp, 3, vp, 0, vp, 1, 3, 100, 0, 0, vp, vp, vp, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
     assert f(None, 0, None, 0, None, 0, 3, 100, 0, 0, None, None, None, None, None, 0, None) == sv.SV_OK
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_sample_and_verify_largest_vocabulary(sv, dt):
+    """V = 2^24, the largest vocabulary the boundary takes: the draft rows are too long to
+    stage, so the streaming sampler draws from them with a cluster wide enough for its
+    tile sums; a sampling row and a greedy row against the oracle."""
+    w = synth.tiny_chain(seed=87, V=1 << 24, K=1, B=2)
+    w["temperature"] = np.array([1.0, 0.0], np.float32)
+    if dt == "bf16":
+        w["target"] = synth.f32_to_bf16_bits(w["target"])
+        w["draft"] = synth.f32_to_bf16_bits(w["draft"])
+    g = _gpu(sv, w, 5, 1)
+    o = oracle.sample_and_verify(w["target"], w["draft"], w["temperature"], 5, 1)
+    assert compare(g, o, keys=("draft_tokens", "tokens", "count")) <= 1
+
+
+def test_sample_and_verify_longest_draft(sv):
+    """K = 64 drafted positions, the most the boundary takes, sampling and greedy rows."""
+    w = synth.tiny_chain(seed=88, V=300, K=64, B=6, sigma=0.05)
+    w["temperature"][::2] = 0.0
+    for seed, offset in [(7, 0), (7, 3)]:
+        g = _gpu(sv, w, seed, offset)
+        o = oracle.sample_and_verify(w["target"], w["draft"], w["temperature"], seed, offset)
+        assert compare(g, o, keys=("draft_tokens", "tokens", "count")) <= 1
