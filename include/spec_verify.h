@@ -170,8 +170,9 @@ SV_API sv_status spec_verify_chain_noalloc(const void *target_logits, sv_dtype t
  *   d_in, d_out    device buffers of in_bytes and out_bytes (spec_verify_host_sizes).
  *   workspace, ws_bytes  as spec_verify_chain.
  * The outputs in h_out are valid once the stream has reached this call's end (an event
- * or a synchronisation).  Alternating two d_in / d_out pairs over two streams overlaps
- * one round's copy with the previous round's verify.  Errors: those of
+ * or a synchronisation).  Independent rounds on several streams in turn, each stream
+ * with its own d_in / d_out pair and workspace, overlap one round's copy with the
+ * verifies (and the copies' fixed start-up latency) of the rounds before it.  Errors: those of
  * spec_verify_chain; SV_ERR_INVALID_ARG for a NULL buffer; SV_ERR_CUDA when a copy cannot
  * be enqueued.
  */
