@@ -12,7 +12,7 @@ sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 
 from speculative_decoding_verification_53_gb300 import synth  # noqa: E402
-from _harness import compare, gpu_chain, oracle_chain, to_dev  # noqa: E402
+from _harness import compare, gpu_chain, oracle_chain  # noqa: E402
 
 
 def main():
