@@ -77,7 +77,7 @@ extern "C" {
 typedef enum {
     SV_OK = 0,
     SV_ERR_INVALID_ARG = 1, /* a size, pointer, dtype or kind argument is invalid */
-    SV_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles (size limits, device) */
+    SV_ERR_UNSUPPORTED = 2, /* valid but outside what the library handles (size limits, device) */
     SV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
     SV_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up on some row (out_count = -1, see
                                spec_verify_rows_status); re-zero the workspace before reusing it */

@@ -426,7 +426,7 @@ const char* spec_verify_status_string(sv_status status) {
     switch (status) {
         case SV_OK: return "SV_OK: success";
         case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG: a size, pointer, dtype or kind argument is invalid";
-        case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED: outside what this build handles";
+        case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED: outside what the library handles";
         case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA runtime call or kernel launch failed";
         case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded device-side wait gave up";
         case SV_ERR_BAD_INPUT: return "SV_ERR_BAD_INPUT: invalid data in a batch row";

@@ -33,7 +33,7 @@ def test_reference_arm_prints_the_contract_line(extra, unit):
 
 def test_both_arms_print_the_same_config():
     """The reference arm's `config` is the one the GPU arm prints for the same workload
-    (both come from one function of the workload), so the driver can compare the arms."""
+    (both come from one function of the workload), so the two lines compare like for like."""
     import argparse
     sys.path.insert(0, ROOT)
     import bench
