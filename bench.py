@@ -332,6 +332,7 @@ class Timed:
             ws_bytes = sv.spec_verify_workspace_size(rows, K_, w["target"].shape[2])
             ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=device)
         n_inputs = self.n_inputs
+        self._chain_inputs = None if (self.tree or self.sample) else (dt, dd, dtok, dtemp, kind, seed)
         # every tensor the captured graphs read or write stays referenced by this object:
         # a graph holds raw device pointers only, so a tensor that went out of scope here
         # would be freed and its memory reused while the graphs still run on it
@@ -426,6 +427,38 @@ class Timed:
                 dense.append(dense_bytes_chain(w, range(r, r + rows)))
         return float(np.mean(alg)), float(np.mean(dense)), float(counts.mean())
 
+    def acceptance(self, max_sets=64):
+        """Per-position acceptance, untimed, for chain workloads with sampling rows: one
+        verify call per input set (at most max_sets) asking for min(1, p_k(x_k)/q_k(x_k)).
+        Its mean over the sampling rows that reached position k estimates
+        alpha_k = sum_x min(p_k(x), q_k(x)), the expected acceptance of a token drawn
+        from q_k; positions after a row's first rejection are not evaluated (-1)."""
+        import torch
+        import speculative_decoding_verification_53_gb300 as sv
+        if self._chain_inputs is None:
+            return None
+        dt, dd, dtok, dtemp, kind, seed = self._chain_inputs
+        rows = self.w["per_step_rows"]
+        sampling = torch.from_numpy(np.asarray(self.w["temperature"]) > 0)
+        if not bool(sampling.any()):
+            return None
+        probs, keep = [], []
+        with torch.cuda.stream(self.stream):
+            for i in range(min(self.n_inputs, max_sets)):
+                sl = slice(i * rows, (i + 1) * rows)
+                _, _, ap = sv.spec_verify_chain(dt[sl], dd[sl], dtok[sl], dtemp[sl], seed, i, draft_kind=kind,
+                                                want_accept_prob=True)
+                probs.append(ap)
+                keep.append(sampling[sl])
+        torch.cuda.synchronize(self.device)
+        ap = torch.cat(probs).cpu().numpy()
+        on = torch.cat(keep).numpy()[:, None] & (ap >= 0)
+        n = on.sum(0)
+        alpha = [float(ap[on[:, k], k].mean()) if n[k] else None for k in range(ap.shape[1])]
+        return {"alpha_per_position": alpha, "rows_per_position": [int(x) for x in n],
+                "estimate": "mean of min(1, p_k(x_k)/q_k(x_k)) over the sampling rows that reached position k "
+                            "(the library's out_accept_prob, one untimed call per input set)"}
+
 
 
 def l2_note(w):
@@ -493,6 +526,9 @@ def run_side_workloads(args, rank, world, device, stream):
                  "unit": "trees/s" if w["kind"] == "tree" else UNIT, "mean_tokens_per_round": mean_count,
                  "l2": l2_note(w), "clocks": clocks,
                  "roofline": roofline_entry(alg, dense, ms, traffic, prof, pk or "kernel chosen by the library")}
+        acc = t.acceptance()
+        if acc is not None:
+            entry["acceptance"] = acc
         if rank == 0 and not args.no_cpu_baseline:
             entry["cpu_baseline"] = run_cpu_baseline(w, w["per_step_rows"], t.n_inputs, w["kind"] == "tree",
                                                      budget_s=4.0)
@@ -520,6 +556,7 @@ def run_ours(args, rank, world, device):
     t = Timed(w, device, stream, args.steps, args.warmup)
     elapsed_ms, clock = t.run(world, device.index if device.index is not None else 0)
     bytes_per_launch, dense_bytes, mean_count = t.bytes_per_launch()
+    acceptance = t.acceptance()
     n_inputs, resident = t.n_inputs, t.resident_bytes
     del t
 
@@ -556,6 +593,7 @@ def run_ours(args, rank, world, device):
         "resident_input_sets": n_inputs,
         "resident_bytes": resident,
         "mean_tokens_per_round": mean_count,
+        "acceptance": acceptance,
         "roofline": roofline_entry(bytes_per_launch, dense_bytes, ms_per_step, traffic, prof,
                                    prof_kernel or ("tree_kernel" if tree else "chain kernel chosen by the library")),
         "e2e": e2e,
