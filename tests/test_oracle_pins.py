@@ -334,6 +334,23 @@ def test_expected_tokens_with_per_position_alpha():
     assert abs(c.mean() - expect) < 4 * c.std() / math.sqrt(n)
 
 
+def test_mean_accept_prob_at_a_position_estimates_its_alpha():
+    """With x_k drawn from q_k, the mean of the reported min(1, p_k(x_k)/q_k(x_k)) is
+    alpha_k = sum_x min(p_k(x), q_k(x)) (sum_x q(x) min(1, p(x)/q(x)) = sum_x min(p, q)).
+    Position 0 is evaluated in every round; at later positions only rounds that reached
+    them report a value, and x_k is drawn independently of earlier decisions, so the
+    conditional mean has the same expectation."""
+    V, K, n = 8, 3, 20000
+    target, draft, toks = _fixed_rows_fresh_drafts(V, K, n, seed=37, sigma=1.0)
+    out = oracle.verify_chain(target, draft, toks, np.ones(n, np.float32), 5, 0)
+    ap = out["accept_prob"].astype(np.float64)
+    for k in range(K):
+        alpha = np.minimum(softmax64(target[0, k]), softmax64(draft[0, k])).sum()
+        got = ap[ap[:, k] >= 0, k]
+        assert len(got) > 1000
+        assert abs(got.mean() - alpha) < 4 * got.std() / math.sqrt(len(got)), (k, got.mean(), alpha)
+
+
 # ---------------------------------------------------------- distribution
 
 def test_tv_distance_first_and_second_token():
