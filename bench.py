@@ -58,6 +58,13 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 
 # ------------------------------------------------------------------ inputs
 
+def large_batch_at(w, T):
+    """The large batch at temperature T: the T = 0.7 workload's logits, with the drafted
+    tokens redrawn at T (the same inputs whether T is the run's workload or a side line)."""
+    from speculative_decoding_verification_53_gb300 import synth
+    return w if T == 0.7 else synth.redraw_tokens(w, T, seed=100 + int(T * 10))
+
+
 def make_workload(name: str, rank: int, rounds: int, batch: int = 0, temperature=None):
     from speculative_decoding_verification_53_gb300 import synth
     seed = 1000 + rank
@@ -68,7 +75,7 @@ def make_workload(name: str, rank: int, rounds: int, batch: int = 0, temperature
     if name == "large_batch":
         B = batch or 256
         T = 0.7 if temperature is None else temperature
-        w = synth.large_batch(seed=seed, temperature=T, sigma=1.0, B=B)
+        w = large_batch_at(synth.large_batch(seed=seed, temperature=0.7, sigma=1.0, B=B), T)
         return dict(w, per_step_rows=B, desc=f"large-batch chain verify B={B} K=8 V=152064 T={T:g}, "
                                              "bf16 target and draft logits, draft noise sigma=1")
     if name == "mixed_batch":
@@ -500,7 +507,6 @@ def run_side_workloads(args, rank, world, device, stream):
     """The other verify workloads, each timed like the headline (same steps, warm-up, L2
     flush) with its roofline and the oracle's bounded CPU baseline."""
     import torch
-    from speculative_decoding_verification_53_gb300 import synth
     out = {}
     large, large_dev = None, None
     gpu = device.index if device.index is not None else 0
@@ -509,8 +515,7 @@ def run_side_workloads(args, rank, world, device, stream):
             if large is None:
                 large = make_workload("large_batch", rank, args.rounds, 0, 0.7)
                 large_dev = {k: to_dev(large[k], device) for k in ("target", "draft")}
-            w = large if T == 0.7 else dict(synth.redraw_tokens(large, T, seed=100 + int(T * 10)),
-                                              desc=large["desc"].replace("T=0.7", f"T={T:g}"))
+            w = large if T == 0.7 else dict(large_batch_at(large, T), desc=large["desc"].replace("T=0.7", f"T={T:g}"))
             dev_inputs = large_dev
         else:
             w = make_workload(name, rank, args.rounds)
@@ -520,7 +525,8 @@ def run_side_workloads(args, rank, world, device, stream):
         max_ms = slowest_rank_ms(elapsed, world, device)
         ms = max_ms / args.steps
         alg, dense, mean_count = t.bytes_per_launch()
-        traffic, prof, pk = profile_traffic(name, default_size=(name != "large_batch" or T == 0.7))
+        # the large batch at another temperature has its own summary (large_batch_T0, large_batch_T1.5)
+        traffic, prof, pk = profile_traffic(key if name == "large_batch" and T != 0.7 else name)
         entry = {"workload": w["desc"], "ms_per_step": ms,
                  "value": whole_job_rate(w["per_step_rows"], args.steps, world, max_ms),
                  "unit": "trees/s" if w["kind"] == "tree" else UNIT, "mean_tokens_per_round": mean_count,
@@ -574,8 +580,11 @@ def run_ours(args, rank, world, device):
         side = run_side_workloads(args, rank, world, device, stream)
     if rank != 0:
         return None
-    traffic, prof, prof_kernel = profile_traffic(args.workload, default_size=not (args.batch or args.temperature is not None
-                                                                               or args.rounds != 64))
+    prof_name = args.workload
+    if args.workload == "large_batch" and args.temperature is not None and args.temperature != 0.7:
+        prof_name = f"large_batch_T{args.temperature:g}"
+    traffic, prof, prof_kernel = profile_traffic(prof_name, default_size=not (args.batch or args.rounds != 64 or (
+        args.temperature is not None and args.workload != "large_batch")))
     line = {
         "metric": METRIC,
         "value": value,
