@@ -50,3 +50,22 @@ def test_both_arms_print_the_same_config():
     assert res.returncode == 0, res.stderr[-2000:]
     line = json.loads(res.stdout.strip().splitlines()[-1])
     assert line["config"] == bench.aux_config(bench.make_aux(args, 0), 1)
+
+
+def test_large_batch_at_another_temperature_is_one_workload():
+    """The large batch at T != 0.7 is the T = 0.7 logits with the drafts redrawn at T,
+    whether it is the run's workload or a side line, so one ncu summary per temperature
+    describes both; each such summary names its own temperature."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    base = bench.make_workload("large_batch", 0, 64, batch=2, temperature=0.7)
+    for T in (0.0, 1.5):
+        run = bench.make_workload("large_batch", 0, 64, batch=2, temperature=T)
+        side = bench.large_batch_at(base, T)
+        for k in ("target", "draft", "tokens", "temperature"):
+            assert np.array_equal(run[k], side[k]), (T, k)
+        assert (run["temperature"] == np.float32(T)).all()
+        traffic, path, kernel = bench.profile_traffic(f"large_batch_T{T:g}")
+        assert path is not None and path.endswith(f"_large_batch_T{T:g}.md") and kernel == "chain_staged_kernel"
+    assert bench.large_batch_at(base, 0.7) is base
