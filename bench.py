@@ -25,7 +25,11 @@ and `roofline.traffic` is the DRAM bytes per launch from the committed ncu
 summary of that kernel (null once the kernel's sources have changed); `e2e` is
 the same metric through the public API with host buffers (copies inside the
 timed region); `cpu_baseline` is the fp64 oracle on a bounded sample, single
-thread.
+thread; `acceptance` (chain workloads with sampling rows) is the mean of the
+library's min(1, p/q) per drafted position, from untimed calls after the timed
+region.  With the default single-stream workload the line also carries
+`workloads`: the large batch at T = 0, 0.7 and 1.5, the mixed batch and the tree,
+each timed the same way.
 """
 from __future__ import annotations
 
